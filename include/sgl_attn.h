@@ -1,0 +1,184 @@
+/*
+ * sgl_attn.h -- C ABI of the GB300 (sm_103a) slot-indexed attention library
+ * (libsgl_attn.so).
+ *
+ * The library computes the data-parallel hot path of prefix-shared attention
+ * over a token-granular KV pool: every token of every request owns one pool
+ * slot, a table req_to_token[request row, position] gives that slot, and two
+ * requests that share a prefix hold identical slot numbers in the leading
+ * entries of their rows ("Inside SGLang", Step 3: Paged KV and the kernels
+ * that read it; "Origins: the paper and the first commit", Memory: a
+ * two-level pool paged by token).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise.
+ *     The caller allocates and owns all buffers; the library never allocates
+ *     or frees device memory and never synchronises the device.
+ *   - Work is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *     The return value reports host-side argument validation and the launch
+ *     status only; it never waits for the kernels.
+ *   - bf16 tensors are dense, row-major, with the last dimension contiguous,
+ *     and must start on a 16-byte boundary.  Indices are int32.
+ *   - Index VALUES held in device memory (slots, req_to_token entries, lengths)
+ *     are not read on the host.  Out-of-range values are undefined behaviour in
+ *     the fast path; the sgl_check_* calls detect them without trapping.
+ *   - head_dim must be 64 or 128; num_q_heads must be a multiple of
+ *     num_kv_heads.  Violations return SGL_ERR_UNSUPPORTED or
+ *     SGL_ERR_INVALID_ARG before anything is launched.
+ */
+#ifndef SGL_ATTN_H
+#define SGL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sgl_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  SGL_OK = 0,
+  SGL_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, negative size */
+  SGL_ERR_UNSUPPORTED = 2, /* head_dim / head-group shape not built */
+  SGL_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  SGL_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+  SGL_ERR_INDEX = 5        /* reported by sgl_check_*: an index value is out of range */
+} sgl_status;
+
+typedef struct {
+  int32_t num_q_heads;  /* Hq */
+  int32_t num_kv_heads; /* Hkv; query head h reads KV head h / (Hq / Hkv) */
+  int32_t head_dim;     /* D: 64 or 128 */
+  int64_t pool_size;    /* S: number of slots in pool_k / pool_v */
+  float sm_scale;       /* softmax scale; 0 selects 1/sqrt(head_dim) */
+} sgl_attn_dims;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sgl_status_string(sgl_status status);
+
+/* Library version, e.g. "0.1.0" (static string). */
+const char* sgl_version(void);
+
+/*
+ * sgl_store_kv -- scatter new keys and values into their pool slots.
+ *
+ * Computes pool_k[slots[i], :, :] = k_new[i, :, :] and
+ *          pool_v[slots[i], :, :] = v_new[i, :, :] for 0 <= i < n,
+ * a bit-exact copy ("Origins: the paper and the first commit", Execution:
+ * store_kv_cache writes the layer's K and V into the key and value buffers
+ * at out_cache_loc).
+ *   k_new, v_new : bf16 [n, Hkv, D]   new rows (read only)
+ *   slots        : int32 [n]          distinct slots in [0, pool_size)
+ *   pool_k/pool_v: bf16 [S, Hkv, D]   written at the n slots only
+ * Duplicate slots are a precondition violation (the last writer is not
+ * defined).  n == 0 is a no-op.
+ */
+sgl_status sgl_store_kv(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
+                        void* pool_k, void* pool_v, const sgl_attn_dims* dims,
+                        sgl_stream_t stream);
+
+/*
+ * sgl_extend_attention -- attention of new suffix tokens over a cached prefix.
+ *
+ * For request r (0 <= r < batch) with prefix length p = prefix_lens[r],
+ * extend length e = extend_lens[r] and row = req_pool_idx[r]:
+ *   keys/values 0..p-1  : pool_k/pool_v[req_to_token[row * rtt_stride + j]]
+ *   keys/values p..p+e-1: k_new/v_new rows of the request's suffix
+ * Suffix query i (0 <= i < e; absolute position p+i) attends to keys
+ * 0..p+i, so the result equals the last e rows of full causal attention over
+ * the p+e tokens ("Inside SGLang", Step 3: Look inside the forward pass --
+ * scores scaled by 1/sqrt(head_dim), keys after the query masked, softmax,
+ * times V; "Origins", Batching: EXTEND computes only the new suffix after the
+ * cached prefix, seq_len = prefix + extend).
+ *   q            : bf16 [T, Hq, D]    suffix queries of all requests back to
+ *                                    back (request r starts at the exclusive
+ *                                    prefix sum of extend_lens)
+ *   k_new, v_new : bf16 [T, Hkv, D]   suffix keys/values, same order
+ *   pool_k/pool_v: bf16 [S, Hkv, D]   read at prefix slots only (never written)
+ *   req_to_token : int32 [rtt_rows, rtt_stride]
+ *   req_pool_idx, prefix_lens, extend_lens: int32 [batch]
+ *   total_extend : T = sum(extend_lens)  (host value; sizes the launch)
+ *   max_extend   : >= max(extend_lens)   (host value)
+ *   max_prefix   : >= max(prefix_lens)   (host value; informational)
+ *   out          : bf16 [T, Hq, D]    written for every suffix row
+ *   workspace    : device buffer of at least sgl_extend_workspace_bytes();
+ *                  it must be zero-filled once before first use.  Word 0 is
+ *                  set to a nonzero code if a bounded on-chip wait gave up
+ *                  (the output is then incomplete); it is never cleared by
+ *                  the library.
+ * Softmax is computed in fp32 from fp32 tensor-core accumulators; out is
+ * rounded to bf16 (nearest even).
+ */
+sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_new,
+                                const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                                int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
+                                size_t workspace_bytes, const sgl_attn_dims* dims,
+                                sgl_stream_t stream);
+
+/*
+ * sgl_decode_attention -- one query per request over all of its slots.
+ *
+ * out[r, h] = softmax_j(scale * q[r, h] . K_j) . V_j over j < seq_lens[r],
+ * K_j/V_j = pool rows at req_to_token[req_pool_idx[r] * rtt_stride + j]
+ * ("Inside SGLang", Step 3: decode reads the key and value of every earlier
+ * token).  seq_lens[r] counts the new token, whose K/V sgl_store_kv must
+ * have written first (decode equals extend with extend_len = 1).
+ *   q            : bf16 [batch, Hq, D]
+ *   seq_lens     : int32 [batch], each >= 1
+ *   max_seq_len  : >= max(seq_lens) (host value; sizes the split-KV schedule)
+ *   out          : bf16 [batch, Hq, D]
+ *   workspace    : >= sgl_decode_workspace_bytes(batch, max_seq_len, dims);
+ *                  scratch for the split-KV partial results.
+ * The keys of a request are split into chunks processed in parallel; each
+ * chunk keeps an fp32 online-softmax state (max, sum, weighted V sum) and a
+ * second kernel merges the chunks of requests that have more than one.
+ */
+sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* seq_lens,
+                                int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                                size_t workspace_bytes, const sgl_attn_dims* dims,
+                                sgl_stream_t stream);
+
+/* Workspace sizes (host only; no device call). */
+size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims);
+size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_attn_dims* dims);
+
+/*
+ * Checked mode.  Each call validates the index values in device memory with a
+ * kernel that never traps: it writes into d_error (int32[4], device) the
+ * first violation found as {kind, a, b, c} and leaves d_error untouched when
+ * everything is in range.  The caller zeroes d_error beforehand and reads it
+ * after the stream completes; kind != 0 means SGL_ERR_INDEX.
+ *   kind 1: slot out of [0, pool_size)          a = list/row index, b = position, c = value
+ *   kind 2: req_pool_idx out of [0, rtt_rows)   a = request, c = value
+ *   kind 3: length negative / seq_len < 1        a = request, c = value
+ *   kind 4: prefix+extend or seq_len > rtt_stride  a = request, c = length
+ *   kind 5: sum(extend_lens) != total_extend or a length above the host max
+ *   kind 6: duplicate slot in one store_kv call  a = second index, c = slot
+ * sgl_check_store_kv_indices needs a scratch bitmap of (pool_size+7)/8 bytes
+ * (rounded up to 16) in `bitmap`; it is cleared by the call.
+ */
+sgl_status sgl_check_store_kv_indices(const int32_t* slots, int32_t n, int64_t pool_size,
+                                      void* bitmap, size_t bitmap_bytes, int32_t* d_error,
+                                      sgl_stream_t stream);
+sgl_status sgl_check_extend_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                    const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                                    int32_t max_extend, int32_t max_prefix, int64_t pool_size,
+                                    int32_t* d_error, sgl_stream_t stream);
+sgl_status sgl_check_decode_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* seq_lens,
+                                    int32_t batch, int32_t max_seq_len, int64_t pool_size,
+                                    int32_t* d_error, sgl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGL_ATTN_H */

@@ -1,0 +1,188 @@
+"""Thin ctypes binding of libsgl_attn.so (names follow the C ABI).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (PyTorch provides device memory and streams);
+bf16 tensors are ``torch.bfloat16``, indices ``torch.int32``.  A call that
+the library rejects raises ``SglError``.  If the library is missing it is
+built from source with nvcc; if that is impossible the import fails loudly --
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+c_i32, c_i64, c_f32, c_size, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+STATUS = {0: "SGL_OK", 1: "SGL_ERR_INVALID_ARG", 2: "SGL_ERR_UNSUPPORTED", 3: "SGL_ERR_WORKSPACE",
+          4: "SGL_ERR_CUDA", 5: "SGL_ERR_INDEX"}
+
+
+class SglError(RuntimeError):
+    def __init__(self, func: str, code: int):
+        super().__init__(f"{func} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class sgl_attn_dims(ctypes.Structure):
+    _fields_ = [("num_q_heads", c_i32), ("num_kv_heads", c_i32), ("head_dim", c_i32),
+                ("pool_size", c_i64), ("sm_scale", c_f32)]
+
+
+_P = ctypes.POINTER
+_SIGS = {
+    "sgl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "sgl_version": (ctypes.c_char_p, []),
+    "sgl_store_kv": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, _P(sgl_attn_dims), c_vp]),
+    "sgl_extend_attention": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp,
+                                            c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_size,
+                                            _P(sgl_attn_dims), c_vp]),
+    "sgl_decode_attention": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_i32,
+                                            c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims), c_vp]),
+    "sgl_extend_workspace_bytes": (c_size, [c_i32, c_i32, _P(sgl_attn_dims)]),
+    "sgl_decode_workspace_bytes": (c_size, [c_i32, c_i32, _P(sgl_attn_dims)]),
+    "sgl_check_store_kv_indices": (ctypes.c_int, [c_vp, c_i32, c_i64, c_vp, c_size, c_vp, c_vp]),
+    "sgl_check_extend_indices": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
+                                                c_i32, c_i64, c_vp, c_vp]),
+    "sgl_check_decode_indices": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i64,
+                                                c_vp, c_vp]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if needed) the C-ABI library."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path) or os.environ.get("SGL_ATTN_REBUILD"):
+            path = _build.build()
+        cdll = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(cdll, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = cdll
+    return _lib
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def _check(name: str, code: int) -> None:
+    if code != 0:
+        raise SglError(name, code)
+
+
+def make_dims(num_q_heads, num_kv_heads, head_dim, pool_size, sm_scale=0.0) -> sgl_attn_dims:
+    return sgl_attn_dims(int(num_q_heads), int(num_kv_heads), int(head_dim), int(pool_size), float(sm_scale))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dims_for(q_or_new, pool_k, sm_scale):
+    return make_dims(q_or_new.shape[1] if q_or_new is not None else pool_k.shape[1],
+                     pool_k.shape[1], pool_k.shape[2], pool_k.shape[0], sm_scale)
+
+
+# ----------------------------------------------------------------- calls
+
+def sgl_store_kv(k_new, v_new, slots, pool_k, pool_v, stream=None):
+    """pool_k[slots[i]] = k_new[i]; pool_v[slots[i]] = v_new[i]."""
+    d = make_dims(pool_k.shape[1], pool_k.shape[1], pool_k.shape[2], pool_k.shape[0])
+    _check("sgl_store_kv", lib().sgl_store_kv(_ptr(k_new), _ptr(v_new), _ptr(slots), int(slots.shape[0]),
+                                              _ptr(pool_k), _ptr(pool_v), ctypes.byref(d), _stream(stream)))
+
+
+def extend_workspace_bytes(batch, total_extend, dims: sgl_attn_dims) -> int:
+    return int(lib().sgl_extend_workspace_bytes(int(batch), int(total_extend), ctypes.byref(dims)))
+
+
+def decode_workspace_bytes(batch, max_seq_len, dims: sgl_attn_dims) -> int:
+    return int(lib().sgl_decode_workspace_bytes(int(batch), int(max_seq_len), ctypes.byref(dims)))
+
+
+def new_workspace(nbytes: int, device):
+    """A zero-filled device byte buffer (16-byte aligned by the allocator)."""
+    import torch
+    return torch.zeros(max(16, int(nbytes)), dtype=torch.uint8, device=device)
+
+
+def sgl_extend_attention(q, k_new, v_new, pool_k, pool_v, req_to_token, req_pool_idx, prefix_lens,
+                         extend_lens, out=None, *, max_extend, max_prefix=0, total_extend=None,
+                         workspace=None, sm_scale=0.0, stream=None):
+    """Attention of the suffix tokens over cached prefix + causal suffix.
+
+    ``max_extend``/``max_prefix``/``total_extend`` are host-side values (the
+    library never reads device memory on the host)."""
+    import torch
+    T = int(q.shape[0]) if total_extend is None else int(total_extend)
+    d = _dims_for(q, pool_k, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    B = int(req_pool_idx.shape[0])
+    if workspace is None:
+        workspace = new_workspace(extend_workspace_bytes(B, T, d), q.device)
+    _check("sgl_extend_attention", lib().sgl_extend_attention(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pool_k), _ptr(pool_v), _ptr(req_to_token),
+        int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(prefix_lens),
+        _ptr(extend_lens), B, T, int(max_extend), int(max_prefix), _ptr(out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), ctypes.byref(d), _stream(stream)))
+    return out
+
+
+def sgl_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_lens, out=None, *,
+                         max_seq_len, workspace=None, sm_scale=0.0, stream=None):
+    """One query per request over all ``seq_len`` keys of its row."""
+    import torch
+    d = _dims_for(q, pool_k, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    B = int(q.shape[0])
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_bytes(B, max_seq_len, d), q.device)
+    _check("sgl_decode_attention", lib().sgl_decode_attention(
+        _ptr(q), _ptr(pool_k), _ptr(pool_v), _ptr(req_to_token), int(req_to_token.shape[0]),
+        int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(seq_lens), B, int(max_seq_len), _ptr(out),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()), ctypes.byref(d),
+        _stream(stream)))
+    return out
+
+
+def sgl_check_store_kv_indices(slots, pool_size, d_error, bitmap=None, stream=None):
+    import torch
+    need = ((int(pool_size) + 31) // 32 * 4 + 15) // 16 * 16
+    if bitmap is None:
+        bitmap = torch.empty(need, dtype=torch.uint8, device=slots.device)
+    _check("sgl_check_store_kv_indices", lib().sgl_check_store_kv_indices(
+        _ptr(slots), int(slots.shape[0]), int(pool_size), _ptr(bitmap),
+        int(bitmap.numel()), _ptr(d_error), _stream(stream)))
+
+
+def sgl_check_extend_indices(req_to_token, req_pool_idx, prefix_lens, extend_lens, *, total_extend,
+                             max_extend, max_prefix, pool_size, d_error, stream=None):
+    _check("sgl_check_extend_indices", lib().sgl_check_extend_indices(
+        _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx),
+        _ptr(prefix_lens), _ptr(extend_lens), int(req_pool_idx.shape[0]), int(total_extend),
+        int(max_extend), int(max_prefix), int(pool_size), _ptr(d_error), _stream(stream)))
+
+
+def sgl_check_decode_indices(req_to_token, req_pool_idx, seq_lens, *, max_seq_len, pool_size, d_error,
+                             stream=None):
+    _check("sgl_check_decode_indices", lib().sgl_check_decode_indices(
+        _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx),
+        _ptr(seq_lens), int(req_pool_idx.shape[0]), int(max_seq_len), int(pool_size), _ptr(d_error),
+        _stream(stream)))

@@ -1,0 +1,314 @@
+// C ABI of libsgl_attn.so: host-side argument validation, workspace sizing,
+// dispatch to the kernel launchers, and the checked-mode index validators.
+// Nothing here allocates device memory or synchronises the device.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace sgl {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates dims and fills the effective scale; returns SGL_OK or an error.
+sgl_status check_dims(const sgl_attn_dims* d, float* scale) {
+  if (d == nullptr) return SGL_ERR_INVALID_ARG;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->pool_size <= 0) return SGL_ERR_INVALID_ARG;
+  if (d->num_q_heads % d->num_kv_heads != 0) return SGL_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return SGL_ERR_UNSUPPORTED;
+  if (!(d->sm_scale >= 0.f) || isinf(d->sm_scale)) return SGL_ERR_INVALID_ARG;
+  *scale = d->sm_scale > 0.f ? d->sm_scale : 1.0f / sqrtf((float)d->head_dim);
+  return SGL_OK;
+}
+
+__device__ void report(int32_t* err, int32_t kind, int32_t a, int32_t b, int32_t c) {
+  if (atomicCAS(err, 0, kind) == 0) {
+    err[1] = a;
+    err[2] = b;
+    err[3] = c;
+  }
+}
+
+__global__ void check_store_kernel(const int32_t* __restrict__ slots, int32_t n, int64_t S,
+                                   uint32_t* __restrict__ bitmap, int32_t* err) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t s = slots[i];
+    if (s < 0 || s >= S) {
+      report(err, 1, (int32_t)i, 0, s);
+      continue;
+    }
+    const uint32_t bit = 1u << (s & 31);
+    const uint32_t old = atomicOr(&bitmap[s >> 5], bit);
+    if (old & bit) report(err, 6, (int32_t)i, 0, s);
+  }
+}
+
+// mode 0: extend (lens_a = prefix, lens_b = extend); mode 1: decode (lens_a = seq)
+__global__ void check_rows_kernel(const int32_t* __restrict__ rtt, int32_t rtt_rows, int32_t stride,
+                                  const int32_t* __restrict__ rpi, const int32_t* __restrict__ lens_a,
+                                  const int32_t* __restrict__ lens_b, int32_t mode, int64_t S,
+                                  int32_t max_a, int32_t max_b, int32_t* err) {
+  const int r = blockIdx.x;
+  const int32_t row = rpi[r];
+  if (row < 0 || row >= rtt_rows) {
+    if (threadIdx.x == 0) report(err, 2, r, 0, row);
+    return;
+  }
+  int32_t n;
+  if (mode == 0) {
+    const int32_t pl = lens_a[r], el = lens_b[r];
+    if (pl < 0 || el < 0) {
+      if (threadIdx.x == 0) report(err, 3, r, 0, pl < 0 ? pl : el);
+      return;
+    }
+    if ((int64_t)pl + el > stride) {
+      if (threadIdx.x == 0) report(err, 4, r, 0, pl + el);
+      return;
+    }
+    if (pl > max_a || el > max_b) {
+      if (threadIdx.x == 0) report(err, 5, r, 0, pl > max_a ? pl : el);
+      return;
+    }
+    n = pl;
+  } else {
+    const int32_t sl = lens_a[r];
+    if (sl < 1) {
+      if (threadIdx.x == 0) report(err, 3, r, 0, sl);
+      return;
+    }
+    if (sl > stride) {
+      if (threadIdx.x == 0) report(err, 4, r, 0, sl);
+      return;
+    }
+    if (sl > max_a) {
+      if (threadIdx.x == 0) report(err, 5, r, 0, sl);
+      return;
+    }
+    n = sl;
+  }
+  const int32_t* row_p = rtt + (int64_t)row * stride;
+  for (int32_t j = threadIdx.x; j < n; j += blockDim.x) {
+    const int32_t s = row_p[j];
+    if (s < 0 || s >= S) report(err, 1, r, j, s);
+  }
+}
+
+__global__ void check_sum_kernel(const int32_t* __restrict__ lens, int32_t batch, int32_t total,
+                                 int32_t* err) {
+  __shared__ long long part[32];
+  long long s = 0;
+  for (int i = threadIdx.x; i < batch; i += blockDim.x) s += lens[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += part[w];
+    if (t != total) report(err, 5, -1, (int32_t)t, total);
+  }
+}
+
+sgl_status last_launch() { return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA; }
+
+}  // namespace
+}  // namespace sgl
+
+using namespace sgl;
+
+extern "C" {
+
+const char* sgl_status_string(sgl_status s) {
+  switch (s) {
+    case SGL_OK: return "SGL_OK";
+    case SGL_ERR_INVALID_ARG: return "SGL_ERR_INVALID_ARG";
+    case SGL_ERR_UNSUPPORTED: return "SGL_ERR_UNSUPPORTED";
+    case SGL_ERR_WORKSPACE: return "SGL_ERR_WORKSPACE";
+    case SGL_ERR_CUDA: return "SGL_ERR_CUDA";
+    case SGL_ERR_INDEX: return "SGL_ERR_INDEX";
+  }
+  return "SGL_ERR_UNKNOWN";
+}
+
+const char* sgl_version(void) { return "0.1.0"; }
+
+sgl_status sgl_store_kv(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
+                        void* pool_k, void* pool_v, const sgl_attn_dims* dims,
+                        sgl_stream_t stream) {
+  float scale;
+  sgl_status st = check_dims(dims, &scale);
+  if (st != SGL_OK) return st;
+  if (n < 0) return SGL_ERR_INVALID_ARG;
+  if (n == 0) return SGL_OK;
+  if (!k_new || !v_new || !slots || !pool_k || !pool_v) return SGL_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) || !aligned16(pool_v))
+    return SGL_ERR_INVALID_ARG;
+  if ((int64_t)n > dims->pool_size) return SGL_ERR_INVALID_ARG;  // slots must be distinct
+  const int32_t row_bytes = dims->num_kv_heads * dims->head_dim * 2;
+  return launch_store_kv(k_new, v_new, slots, n, pool_k, pool_v, row_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims) {
+  (void)batch;
+  (void)total_extend;
+  (void)dims;
+  return extend_workspace_bytes();
+}
+
+size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_attn_dims* dims) {
+  if (dims == nullptr || dims->num_kv_heads <= 0 || dims->num_q_heads <= 0) return 0;
+  return decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads, dims->num_kv_heads,
+                                dims->head_dim);
+}
+
+sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_new,
+                                const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                                int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
+                                size_t workspace_bytes, const sgl_attn_dims* dims,
+                                sgl_stream_t stream) {
+  float scale;
+  sgl_status st = check_dims(dims, &scale);
+  if (st != SGL_OK) return st;
+  if (batch < 0 || total_extend < 0 || max_extend < 0 || max_prefix < 0) return SGL_ERR_INVALID_ARG;
+  if (batch == 0 || total_extend == 0) return SGL_OK;
+  if (!q || !k_new || !v_new || !pool_k || !pool_v || !req_to_token || !req_pool_idx ||
+      !prefix_lens || !extend_lens || !out)
+    return SGL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) ||
+      !aligned16(pool_v) || !aligned16(out))
+    return SGL_ERR_INVALID_ARG;
+  if (rtt_rows <= 0 || rtt_stride <= 0 || max_extend > total_extend) return SGL_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < extend_workspace_bytes() || !aligned16(workspace))
+    return SGL_ERR_WORKSPACE;
+  ExtendArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.req_to_token = req_to_token;
+  a.rtt_stride = rtt_stride;
+  a.req_pool_idx = req_pool_idx;
+  a.prefix_lens = prefix_lens;
+  a.extend_lens = extend_lens;
+  a.batch = batch;
+  a.total_extend = total_extend;
+  a.max_extend = max_extend;
+  a.out = out;
+  a.workspace = workspace;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.head_dim = dims->head_dim;
+  a.sm_scale = scale;
+  return launch_extend(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* seq_lens,
+                                int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                                size_t workspace_bytes, const sgl_attn_dims* dims,
+                                sgl_stream_t stream) {
+  float scale;
+  sgl_status st = check_dims(dims, &scale);
+  if (st != SGL_OK) return st;
+  if (batch < 0 || max_seq_len < 0) return SGL_ERR_INVALID_ARG;
+  if (batch == 0) return SGL_OK;
+  if (max_seq_len < 1) return SGL_ERR_INVALID_ARG;
+  if (!q || !pool_k || !pool_v || !req_to_token || !req_pool_idx || !seq_lens || !out)
+    return SGL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool_k) || !aligned16(pool_v)) return SGL_ERR_INVALID_ARG;
+  if (rtt_rows <= 0 || rtt_stride <= 0) return SGL_ERR_INVALID_ARG;
+  const size_t need = decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads,
+                                             dims->num_kv_heads, dims->head_dim);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return SGL_ERR_WORKSPACE;
+  DecodeArgs a;
+  a.q = q;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.req_to_token = req_to_token;
+  a.rtt_stride = rtt_stride;
+  a.req_pool_idx = req_pool_idx;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_seq_len = max_seq_len;
+  a.out = out;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.head_dim = dims->head_dim;
+  a.sm_scale = scale;
+  return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgl_status sgl_check_store_kv_indices(const int32_t* slots, int32_t n, int64_t pool_size,
+                                      void* bitmap, size_t bitmap_bytes, int32_t* d_error,
+                                      sgl_stream_t stream) {
+  if (n < 0 || pool_size <= 0 || d_error == nullptr) return SGL_ERR_INVALID_ARG;
+  if (n == 0) return SGL_OK;
+  if (slots == nullptr) return SGL_ERR_INVALID_ARG;
+  const size_t need = (((size_t)pool_size + 31) / 32 * 4 + 15) / 16 * 16;
+  if (bitmap == nullptr || bitmap_bytes < need) return SGL_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(bitmap, 0, need, s) != cudaSuccess) return SGL_ERR_CUDA;
+  int64_t blocks = ((int64_t)n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  check_store_kernel<<<(unsigned)blocks, 256, 0, s>>>(slots, n, pool_size,
+                                                      static_cast<uint32_t*>(bitmap), d_error);
+  return last_launch();
+}
+
+sgl_status sgl_check_extend_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                    const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                                    int32_t max_extend, int32_t max_prefix, int64_t pool_size,
+                                    int32_t* d_error, sgl_stream_t stream) {
+  if (batch < 0 || rtt_rows <= 0 || rtt_stride <= 0 || pool_size <= 0 || d_error == nullptr)
+    return SGL_ERR_INVALID_ARG;
+  if (batch == 0) return SGL_OK;
+  if (!req_to_token || !req_pool_idx || !prefix_lens || !extend_lens) return SGL_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  check_rows_kernel<<<(unsigned)batch, 256, 0, s>>>(req_to_token, rtt_rows, rtt_stride, req_pool_idx,
+                                                    prefix_lens, extend_lens, 0, pool_size,
+                                                    max_prefix, max_extend, d_error);
+  check_sum_kernel<<<1, 1024, 0, s>>>(extend_lens, batch, total_extend, d_error);
+  return last_launch();
+}
+
+sgl_status sgl_check_decode_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* seq_lens,
+                                    int32_t batch, int32_t max_seq_len, int64_t pool_size,
+                                    int32_t* d_error, sgl_stream_t stream) {
+  if (batch < 0 || rtt_rows <= 0 || rtt_stride <= 0 || pool_size <= 0 || d_error == nullptr)
+    return SGL_ERR_INVALID_ARG;
+  if (batch == 0) return SGL_OK;
+  if (!req_to_token || !req_pool_idx || !seq_lens) return SGL_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  check_rows_kernel<<<(unsigned)batch, 256, 0, s>>>(req_to_token, rtt_rows, rtt_stride, req_pool_idx,
+                                                    seq_lens, nullptr, 1, pool_size, max_seq_len, 0,
+                                                    d_error);
+  return last_launch();
+}
+
+}  // extern "C"

@@ -1,0 +1,464 @@
+// Paged decode attention: one query per request over all of its slots.
+//
+// "Inside SGLang", Step 3 (Prefill and decode have different shapes): a
+// decode step reads the key and value of every earlier token, so it is bound
+// by memory bandwidth; (Paged KV and the kernels that read it): the kernel
+// reads the request's slot indices from req_to_token and gathers its keys and
+// values from wherever they sit in the pool.
+//
+// Schedule (split-KV):
+//   1. plan    -- one block lists the work items (request, split), a split
+//                 being up to kChunk consecutive keys of one request;
+//   2. split   -- a persistent grid (x: work items, strided; y: KV head) runs
+//                 each item: the slot indices go to shared memory, K and V
+//                 rows of the KV head are gathered by 16-byte cp.async into a
+//                 kStages-deep ring of kTile-key tiles, and the query heads of
+//                 the group share every loaded row.  LPT (8 or 16) lanes own one
+//                 key, each lane a slice of the head dim; every lane group keeps its own
+//                 fp32 online-softmax state (max, sum, weighted V sum) with
+//                 warp-shuffle reductions, and the groups and warps are merged
+//                 at the end of the item.  Requests with one split write the
+//                 output directly; others write their partial state;
+//   3. combine -- one warp per (request, query head) merges the partial
+//                 states of multi-split requests (max-rescaled sums).
+// Scores are kept in the log2 domain (scale * log2(e) folded into q) and the
+// running max is only moved when a score exceeds it by more than 2^8, which
+// keeps every exponentiated weight <= 256 in fp32 and makes rescaling rare.
+#include "common.cuh"
+#include "launch.h"
+
+namespace sgl {
+
+namespace {
+
+constexpr int kChunk = 512;  // keys per work item
+constexpr int kTile = 32;    // keys per pipeline stage
+constexpr int kStages = 4;   // ring depth
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct Ws {
+  int32_t* item_start;  // [B+1]
+  int2* items;          // [max_items]
+  int32_t* n_items;     // [1]
+  float2* part_ml;      // [max_items, Hkv, G]  (max in log2 units, sum)
+  float* part_acc;      // [max_items, Hkv, G, D]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline int64_t max_items_for(int32_t batch, int32_t max_seq_len) {
+  return (int64_t)batch * ((max_seq_len + kChunk - 1) / kChunk);
+}
+
+inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G, int32_t D,
+                        void* base, Ws* ws) {
+  size_t off = 0;
+  size_t o_start = off;
+  off = align256(off + sizeof(int32_t) * (size_t)(batch + 1));
+  size_t o_items = off;
+  off = align256(off + sizeof(int2) * (size_t)max_items);
+  size_t o_n = off;
+  off = align256(off + sizeof(int32_t));
+  size_t o_ml = off;
+  off = align256(off + sizeof(float2) * (size_t)max_items * Hkv * G);
+  size_t o_acc = off;
+  off = align256(off + sizeof(float) * (size_t)max_items * Hkv * G * D);
+  if (ws && base) {
+    char* b = static_cast<char*>(base);
+    ws->item_start = reinterpret_cast<int32_t*>(b + o_start);
+    ws->items = reinterpret_cast<int2*>(b + o_items);
+    ws->n_items = reinterpret_cast<int32_t*>(b + o_n);
+    ws->part_ml = reinterpret_cast<float2*>(b + o_ml);
+    ws->part_acc = reinterpret_cast<float*>(b + o_acc);
+  }
+  return off;
+}
+
+struct Params {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* pool_k;
+  const __nv_bfloat16* pool_v;
+  const int32_t* req_to_token;
+  int64_t rtt_stride;
+  const int32_t* req_pool_idx;
+  const int32_t* seq_lens;
+  __nv_bfloat16* out;
+  int32_t batch, Hq, Hkv;
+  float scale_log2;
+  Ws ws;
+};
+
+// ---------------------------------------------------------------- plan
+
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ seq_lens,
+                                                           int32_t batch, int64_t max_items,
+                                                           Ws ws) {
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (batch + blockDim.x - 1) / blockDim.x;
+  const int r0 = min(batch, tid * per), r1 = min(batch, r0 + per);
+  int32_t local = 0;
+  for (int r = r0; r < r1; ++r) local += (max(seq_lens[r], 0) + kChunk - 1) / kChunk;
+  // block-wide exclusive scan of `local`
+  int32_t inc = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t base = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0);
+  for (int r = r0; r < r1; ++r) {
+    ws.item_start[r] = base;
+    const int32_t ns = (max(seq_lens[r], 0) + kChunk - 1) / kChunk;
+    for (int32_t s = 0; s < ns; ++s)
+      if (base + s < max_items) ws.items[base + s] = make_int2(r, s);
+    base += ns;
+  }
+  if (tid == blockDim.x - 1) {
+    ws.item_start[batch] = base;
+    *ws.n_items = (int32_t)min((int64_t)base, max_items);
+  }
+}
+
+// ---------------------------------------------------------------- split
+
+// LPT lanes own one key; each lane holds D/LPT consecutive-in-16-byte-vectors
+// elements of the head dim.  LPT = 8 for small head groups, 16 when G*D is
+// large (keeps the per-lane query and accumulator registers bounded).
+template <int D, int LPT>
+struct Lane {
+  static constexpr int kVecs = D / (8 * LPT);  // 16-byte vectors per lane per row
+  static constexpr int kElems = kVecs * 8;     // elements per lane
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kRowVecs = D / 8;       // 16-byte vectors per row
+  static constexpr int kGroups = 32 / LPT;     // keys per warp instruction
+  // element offset of vector v of lane li
+  static __device__ __forceinline__ int elem(int v, int li) { return v * (8 * LPT) + li * 8; }
+};
+
+template <int D, int G, int LPT>
+constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
+
+template <int D, int G, int LPT>
+__global__ void __launch_bounds__(kThreads, (min_blocks<D, G, LPT>()))
+decode_split_kernel(Params p) {
+  using L = Lane<D, LPT>;
+  constexpr int EL = L::kElems;
+  constexpr int kTileBytes = kTile * L::kRowBytes;         // one K or V tile
+  constexpr int kStageBytes = 2 * kTileBytes;              // K then V
+  extern __shared__ __align__(128) uint8_t smem[];
+  int32_t* s_slots = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
+  float* s_red = reinterpret_cast<float*>(smem);           // reuses the ring after an item
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane / LPT, li = lane % LPT;
+  const int kvh = blockIdx.y;
+  const int32_t n_items = *p.ws.n_items;
+  const uint32_t ring = smem_u32(smem);
+
+  for (int32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int2 it = p.ws.items[item];
+    const int r = it.x;
+    const int32_t t0 = it.y * kChunk;
+    const int32_t n = min(p.seq_lens[r] - t0, kChunk);
+    const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride + t0;
+    for (int i = tid; i < n; i += kThreads) s_slots[i] = rtt[i];
+
+    // this lane's slice of the G query heads, pre-scaled into log2 units
+    float qf[G][EL];
+    {
+      const __nv_bfloat16* qb = p.q + ((int64_t)r * p.Hq + (int64_t)kvh * G) * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int v = 0; v < L::kVecs; ++v) {
+          uint4 raw = *reinterpret_cast<const uint4*>(qb + h * D + L::elem(v, li));
+          bf16x8_to_f32(raw, &qf[h][v * 8]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qf[h][v * 8 + e] *= p.scale_log2;
+        }
+    }
+    __syncthreads();  // slots visible; previous item's reduction scratch free
+
+    const int n_tiles = (n + kTile - 1) / kTile;
+    const __nv_bfloat16* kbase = p.pool_k + (int64_t)kvh * D;
+    const __nv_bfloat16* vbase = p.pool_v + (int64_t)kvh * D;
+    auto issue = [&](int tile, int stage) {
+      const uint32_t st = ring + stage * kStageBytes;
+      constexpr int kRowsPerPass = kThreads / L::kRowVecs;
+      const int vec = tid % L::kRowVecs;
+#pragma unroll
+      for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
+        const int tok = pass * kRowsPerPass + tid / L::kRowVecs;
+        const int32_t j = tile * kTile + tok;
+        const bool ok = j < n;
+        const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv : 0;
+        const uint32_t d = st + tok * L::kRowBytes + vec * 16;
+        cp_async_16(d, kbase + row * D + vec * 8, ok ? 16u : 0u);
+        cp_async_16(d + kTileBytes, vbase + row * D + vec * 8, ok ? 16u : 0u);
+      }
+    };
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+      if (s < n_tiles) issue(s, s);
+      cp_async_commit();
+    }
+
+    float m[G], l[G], acc[G][EL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EL; ++e) acc[h][e] = 0.f;
+    }
+
+    for (int k = 0; k < n_tiles; ++k) {
+      cp_async_wait<kStages - 2>();
+      __syncthreads();
+      if (k + kStages - 1 < n_tiles) issue(k + kStages - 1, (k + kStages - 1) % kStages);
+      cp_async_commit();
+      const uint8_t* ks = smem + (k % kStages) * kStageBytes;
+      const uint8_t* vs = ks + kTileBytes;
+#pragma unroll
+      for (int sub = 0; sub < kTile / (L::kGroups * kWarps); ++sub) {
+        const int tok = warp * (kTile / kWarps) + sub * L::kGroups + grp;
+        const bool valid = k * kTile + tok < n;
+        float kf[EL];
+#pragma unroll
+        for (int v = 0; v < L::kVecs; ++v)
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(ks + tok * L::kRowBytes + 2 * L::elem(v, li)),
+                        &kf[v * 8]);
+        float s[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < EL; ++e) a = fmaf(qf[h][e], kf[e], a);
+          s[h] = a;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+          for (int o = 1; o < LPT; o <<= 1) s[h] += __shfl_xor_sync(0xffffffffu, s[h], o);
+          if (!valid) s[h] = -INFINITY;
+        }
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < G; ++h) need |= s[h] > m[h] + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if (s[h] > m[h] + kRescaleThreshold) {
+              const float a = ex2(m[h] - s[h]);
+              m[h] = s[h];
+              l[h] *= a;
+#pragma unroll
+              for (int e = 0; e < EL; ++e) acc[h][e] *= a;
+            }
+          }
+        }
+        float vf[EL];
+#pragma unroll
+        for (int v = 0; v < L::kVecs; ++v)
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vs + tok * L::kRowBytes + 2 * L::elem(v, li)),
+                        &vf[v * 8]);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pw = valid ? ex2(s[h] - m[h]) : 0.f;
+          l[h] += pw;
+#pragma unroll
+          for (int e = 0; e < EL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+        }
+      }
+    }
+    cp_async_wait_all();
+
+    // merge the lane groups of the warp (lanes with the same li)
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+        const float mn = fmaxf(m[h], mo);
+        const float fa = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
+        const float fb = mo == -INFINITY ? 0.f : ex2(mo - mn);
+        l[h] = l[h] * fa + lo * fb;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+          const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+          acc[h][e] = acc[h][e] * fa + ao * fb;
+        }
+        m[h] = mn;
+      }
+    }
+    __syncthreads();  // every warp is done with the ring; reuse it for the reduction
+    // s_red layout: [warp][G][D] acc, then [warp][G] m, then [warp][G] l
+    float* red_acc = s_red;
+    float* red_m = s_red + kWarps * G * D;
+    float* red_l = red_m + kWarps * G;
+    if (grp == 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int v = 0; v < L::kVecs; ++v)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_acc[(warp * G + h) * D + L::elem(v, li) + e] = acc[h][v * 8 + e];
+        if (li == 0) {
+          red_m[warp * G + h] = m[h];
+          red_l[warp * G + h] = l[h];
+        }
+      }
+    }
+    __syncthreads();
+    const int32_t s0 = p.ws.item_start[r];
+    const bool single = (p.ws.item_start[r + 1] - s0) == 1;
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      const int h = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * G + h]);
+      float Ls = 0.f, A = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = red_m[w * G + h];
+        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+        Ls += red_l[w * G + h] * f;
+        A += red_acc[(w * G + h) * D + d] * f;
+      }
+      if (single) {
+        p.out[((int64_t)r * p.Hq + (int64_t)kvh * G + h) * D + d] = __float2bfloat16_rn(A / Ls);
+      } else {
+        const int64_t slot = ((int64_t)item * p.Hkv + kvh) * G + h;
+        p.ws.part_acc[slot * D + d] = A;
+        if (d == 0) p.ws.part_ml[slot] = make_float2(M, Ls);
+      }
+    }
+    __syncthreads();  // scratch and slots are rewritten by the next item
+  }
+}
+
+// ---------------------------------------------------------------- combine
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(Params p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (gw >= (int64_t)p.batch * p.Hq) return;
+  const int r = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
+  const int32_t s0 = p.ws.item_start[r];
+  const int32_t ns = p.ws.item_start[r + 1] - s0;
+  if (ns <= 1 || s0 + ns > *p.ws.n_items) return;  // single split, or lengths above max_seq_len
+  const int G = p.Hq / p.Hkv;
+  const int kvh = h / G, hh = h % G;
+  auto slot_of = [&](int32_t s) { return ((int64_t)(s0 + s) * p.Hkv + kvh) * G + hh; };
+  float M = -INFINITY;
+  for (int32_t s = lane; s < ns; s += 32) M = fmaxf(M, p.ws.part_ml[slot_of(s)].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  constexpr int E = D / 32;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float Ls = 0.f;
+  for (int32_t s = 0; s < ns; ++s) {
+    const int64_t sl = slot_of(s);
+    const float2 ml = p.ws.part_ml[sl];
+    const float f = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+    Ls += ml.y * f;
+    const float* a = p.ws.part_acc + sl * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(f, a[lane + 32 * e], acc[e]);
+  }
+  const float inv = 1.f / Ls;
+  __nv_bfloat16* o = p.out + ((int64_t)r * p.Hq + h) * D;
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+}
+
+template <int D, int G>
+sgl_status run(const Params& prm, int64_t max_items, cudaStream_t stream) {
+  constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
+  constexpr size_t smem = (size_t)kStages * 2 * kTile * D * 2 + kChunk * sizeof(int32_t);
+  static_assert(kWarps * G * (D + 2) * sizeof(float) <= (size_t)kStages * 2 * kTile * D * 2,
+                "reduction scratch must fit in the ring");
+  auto kern = decode_split_kernel<D, G, LPT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SGL_ERR_CUDA;
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.ws);
+  int blocks_per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, kThreads, smem) !=
+          cudaSuccess ||
+      blocks_per_sm < 1)
+    blocks_per_sm = 1;
+  int64_t gx = ((int64_t)2 * blocks_per_sm * num_sms() + prm.Hkv - 1) / prm.Hkv;
+  if (gx > max_items) gx = max_items;
+  if (gx < 1) gx = 1;
+  kern<<<dim3((unsigned)gx, (unsigned)prm.Hkv), kThreads, smem, stream>>>(prm);
+  const int64_t warps = (int64_t)prm.batch * prm.Hq;
+  decode_combine_kernel<D><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
+}
+
+template <int D>
+sgl_status run_g(int G, const Params& prm, int64_t max_items, cudaStream_t stream) {
+  switch (G) {
+    case 1: return run<D, 1>(prm, max_items, stream);
+    case 2: return run<D, 2>(prm, max_items, stream);
+    case 4: return run<D, 4>(prm, max_items, stream);
+    case 8: return run<D, 8>(prm, max_items, stream);
+    default: return SGL_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, int32_t Hkv,
+                              int32_t D) {
+  if (batch <= 0 || max_seq_len <= 0 || Hkv <= 0) return 256;
+  return ws_layout(batch, max_items_for(batch, max_seq_len), Hkv, Hq / Hkv, D, nullptr, nullptr);
+}
+
+sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.batch == 0) return SGL_OK;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return SGL_ERR_UNSUPPORTED;
+  const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
+  Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.pool_k = static_cast<const __nv_bfloat16*>(a.pool_k);
+  prm.pool_v = static_cast<const __nv_bfloat16*>(a.pool_v);
+  prm.req_to_token = a.req_to_token;
+  prm.rtt_stride = a.rtt_stride;
+  prm.req_pool_idx = a.req_pool_idx;
+  prm.seq_lens = a.seq_lens;
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.batch = a.batch;
+  prm.Hq = a.num_q_heads;
+  prm.Hkv = a.num_kv_heads;
+  prm.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  const size_t need = ws_layout(a.batch, max_items, a.num_kv_heads, G, a.head_dim, a.workspace, &prm.ws);
+  if (a.workspace == nullptr || a.workspace_bytes < need) return SGL_ERR_WORKSPACE;
+  if (a.head_dim == 128) return run_g<128>(G, prm, max_items, stream);
+  if (a.head_dim == 64) return run_g<64>(G, prm, max_items, stream);
+  return SGL_ERR_UNSUPPORTED;
+}
+
+}  // namespace sgl

@@ -1,0 +1,57 @@
+// Host-side launchers (one per kernel family) and device queries.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sgl_attn.h"
+
+namespace sgl {
+
+// SM count of the current device (cached per device).
+int num_sms();
+
+sgl_status launch_store_kv(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
+                           void* pool_k, void* pool_v, int32_t row_bytes, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;
+  const void* pool_k;
+  const void* pool_v;
+  const int32_t* req_to_token;
+  int32_t rtt_stride;
+  const int32_t* req_pool_idx;
+  const int32_t* seq_lens;
+  int32_t batch, max_seq_len;
+  void* out;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t num_q_heads, num_kv_heads, head_dim;
+  float sm_scale;
+};
+size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim);
+sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+struct ExtendArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const void* pool_k;
+  const void* pool_v;
+  const int32_t* req_to_token;
+  int32_t rtt_stride;
+  const int32_t* req_pool_idx;
+  const int32_t* prefix_lens;
+  const int32_t* extend_lens;
+  int32_t batch, total_extend, max_extend;
+  void* out;
+  void* workspace;
+  int32_t num_q_heads, num_kv_heads, head_dim;
+  float sm_scale;
+};
+size_t extend_workspace_bytes();
+sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream);
+
+}  // namespace sgl

@@ -1,0 +1,129 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-side validation rejects bad arguments before anything is launched.
+No test here touches a GPU (fake, never-dereferenced device pointers are
+only passed to calls that must fail validation first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from radixattention_prefix_shared_gb300 import binding as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "sgl_attn.h")
+
+FAKE = ctypes.c_void_p(0x100000)     # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x100008)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sgl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sgl_store_kv", "sgl_extend_attention", "sgl_decode_attention"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    for name in declared_functions():
+        assert hasattr(cuda_lib, name), f"{name} declared in sgl_attn.h but not exported"
+
+
+def test_status_strings_and_version(cuda_lib):
+    for code, name in B.STATUS.items():
+        assert cuda_lib.sgl_status_string(code).decode() == name
+    assert cuda_lib.sgl_status_string(99).decode() == "SGL_ERR_UNKNOWN"
+    assert re.match(r"^\d+\.\d+\.\d+$", cuda_lib.sgl_version().decode())
+
+
+def test_dims_struct_layout_matches_header():
+    # int32 x3, int64 (8-aligned), float -> 32 bytes with padding
+    assert ctypes.sizeof(B.sgl_attn_dims) == 32
+    assert B.sgl_attn_dims.pool_size.offset == 16 and B.sgl_attn_dims.sm_scale.offset == 24
+
+
+def _dims(**kw):
+    d = dict(num_q_heads=4, num_kv_heads=2, head_dim=128, pool_size=1024, sm_scale=0.0)
+    d.update(kw)
+    return B.make_dims(**d)
+
+
+def test_store_kv_validation(cuda_lib):
+    f = cuda_lib.sgl_store_kv
+    d = _dims()
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, None) == 1                        # dims NULL
+    assert f(FAKE, FAKE, FAKE, -1, FAKE, FAKE, ctypes.byref(d), None) == 1            # n < 0
+    assert f(None, None, None, 0, None, None, ctypes.byref(d), None) == 0             # n == 0: no-op
+    assert f(None, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(d), None) == 1             # null k_new
+    assert f(MISALIGNED, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(d), None) == 1       # misaligned
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(_dims(head_dim=96)), None) == 2
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(_dims(num_q_heads=3)), None) == 1
+    assert f(FAKE, FAKE, FAKE, 2048, FAKE, FAKE, ctypes.byref(d), None) == 1          # n > pool
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(_dims(sm_scale=-1.0)), None) == 1
+
+
+def _extend(cuda_lib, d, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, pk=FAKE, pv=FAKE, rtt=FAKE, rows=4, stride=64, rpi=FAKE,
+             pl=FAKE, el=FAKE, batch=2, total=10, max_e=6, max_p=30, out=FAKE, ws=FAKE, wsb=256)
+    a.update(kw)
+    return cuda_lib.sgl_extend_attention(a["q"], a["k"], a["v"], a["pk"], a["pv"], a["rtt"], a["rows"],
+                                         a["stride"], a["rpi"], a["pl"], a["el"], a["batch"], a["total"],
+                                         a["max_e"], a["max_p"], a["out"], a["ws"], a["wsb"],
+                                         ctypes.byref(d), None)
+
+
+def test_extend_validation(cuda_lib):
+    d = _dims()
+    assert _extend(cuda_lib, d, batch=0) == 0
+    assert _extend(cuda_lib, d, total=0) == 0
+    assert _extend(cuda_lib, d, batch=-1) == 1
+    assert _extend(cuda_lib, d, q=None) == 1
+    assert _extend(cuda_lib, d, out=MISALIGNED) == 1
+    assert _extend(cuda_lib, d, stride=0) == 1
+    assert _extend(cuda_lib, d, max_e=11) == 1          # max_extend above total_extend
+    assert _extend(cuda_lib, d, ws=None) == 3
+    assert _extend(cuda_lib, d, wsb=16) == 3
+    assert _extend(cuda_lib, _dims(head_dim=32)) == 2
+
+
+def test_decode_validation_and_workspace_size(cuda_lib):
+    d = _dims(num_q_heads=16, num_kv_heads=8)
+    need = B.decode_workspace_bytes(248, 32768, d)
+    assert need > 248 * 64 * 8 * 2 * 128 * 4       # partial accumulators dominate
+    f = cuda_lib.sgl_decode_attention
+
+    def call(**kw):
+        a = dict(q=FAKE, pk=FAKE, pv=FAKE, rtt=FAKE, rows=4, stride=64, rpi=FAKE, sl=FAKE, batch=2,
+                 max_s=64, out=FAKE, ws=FAKE, wsb=need)
+        a.update(kw)
+        return f(a["q"], a["pk"], a["pv"], a["rtt"], a["rows"], a["stride"], a["rpi"], a["sl"],
+                 a["batch"], a["max_s"], a["out"], a["ws"], a["wsb"], ctypes.byref(d), None)
+    assert call(batch=0) == 0
+    assert call(max_s=0) == 1
+    assert call(sl=None) == 1
+    assert call(ws=None) == 3
+    assert call(wsb=B.decode_workspace_bytes(2, 64, d) - 1) == 3
+    assert B.extend_workspace_bytes(8, 16384, d) >= 16
+
+
+def test_check_calls_validate_on_host(cuda_lib):
+    assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, None, None) == 1
+    assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, FAKE, None) == 3  # bitmap small
+    assert cuda_lib.sgl_check_store_kv_indices(FAKE, 0, 1024, None, 0, FAKE, None) == 0
+    assert cuda_lib.sgl_check_decode_indices(FAKE, 0, 64, FAKE, FAKE, 2, 64, 1024, FAKE, None) == 1
+    assert cuda_lib.sgl_check_extend_indices(FAKE, 4, 64, FAKE, FAKE, FAKE, 0, 0, 0, 0, 1024, FAKE, None) == 0
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle, and its binding has no
+    non-CUDA code path."""
+    pkg = os.path.dirname(B.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                src = open(os.path.join(root, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f

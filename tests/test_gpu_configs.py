@@ -1,0 +1,99 @@
+"""The five workloads at full size, launched as bench.py launches them.
+
+Outputs are checked on sampled rows that the oracle computes one by one
+(longest and shortest requests, first and last suffix tokens, random ones);
+store_kv is checked bit-exactly on sampled slots; the NaN-poisoned unused
+slots make any stray read visible in every output row.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from radixattention_prefix_shared_gb300 import workloads as W  # noqa: E402
+
+from _gpu import DEV, Run, assert_close, oracle_decode, oracle_extend  # noqa: E402
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+def _sample_requests(seq, k, seed):
+    rng = np.random.default_rng(seed)
+    pick = {int(np.argmax(seq)), int(np.argmin(seq))}
+    pick |= set(int(x) for x in rng.choice(len(seq), size=min(k, len(seq)), replace=False))
+    return sorted(pick)
+
+
+def _sample_tokens(e, k, seed):
+    rng = np.random.default_rng(seed)
+    offs = np.concatenate([[0], np.cumsum(e.extend_lens)])
+    toks = set()
+    for r in range(len(e.extend_lens)):
+        if e.extend_lens[r] > 0:
+            toks |= {int(offs[r]), int(offs[r + 1] - 1)}
+    toks |= set(int(x) for x in rng.integers(0, offs[-1], size=k))
+    return np.array(sorted(toks))
+
+
+def _check_all_finite(bits, what):
+    x = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.isfinite(x).all(), f"{what}: non-finite values (stray read of a poisoned slot?)"
+
+
+def _check_store(run, batch, n=64, seed=0):
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(batch.slots.size, size=min(n, batch.slots.size), replace=False)
+    sl = torch.from_numpy(batch.slots[idx].astype(np.int64)).to(DEV)
+    assert np.array_equal(W.bf16_bits(run.t["pool_k"][sl]), batch.k_new[idx])
+    assert np.array_equal(W.bf16_bits(run.t["pool_v"][sl]), batch.v_new[idx])
+
+
+def test_decode_llama7b_full():
+    w = W.decode_llama7b()
+    run = Run(w)
+    got = run.decode()
+    _check_all_finite(got, "decode")
+    _check_store(run, w.decode[0])
+    reqs = _sample_requests(w.decode[0].seq_lens, 6, 2)
+    want = oracle_decode(w, 0, requests=reqs, pool=w.pool_view(decode_steps=1))
+    assert_close(got[reqs], want, "decode_llama7b")
+
+
+def test_shared_prompt_extend_full():
+    w = W.shared_prompt_extend()
+    run = Run(w)
+    got = run.extend()
+    _check_all_finite(got, "extend")
+    _check_store(run, w.extend)
+    toks = _sample_tokens(w.extend, 24, 3)
+    want = oracle_extend(w, tokens=toks, pool=w.pool_view(with_extend=False))
+    assert_close(got[toks], want, "shared_prompt_extend")
+
+
+def test_tree_of_thought_decode_full():
+    w = W.tree_of_thought_decode()
+    run = Run(w)
+    outs = [run.decode(s) for s in range(len(w.decode))]
+    for s in (0, 8, len(w.decode) - 1):
+        _check_all_finite(outs[s], f"decode step {s}")
+        reqs = _sample_requests(w.decode[s].seq_lens, 5, 10 + s)
+        want = oracle_decode(w, s, requests=reqs, pool=w.pool_view(decode_steps=s + 1))
+        assert_close(outs[s][reqs], want, f"tree decode step {s}")
+    _check_store(run, w.decode[-1])
+
+
+def test_chunked_prefill_mix_full():
+    w = W.chunked_prefill_mix()
+    run = Run(w)
+    ext = run.extend()
+    dec = run.decode()
+    _check_all_finite(ext, "extend")
+    _check_all_finite(dec, "decode")
+    _check_store(run, w.extend)
+    _check_store(run, w.decode[0])
+    pool = w.pool_view(decode_steps=1)
+    toks = _sample_tokens(w.extend, 16, 5)
+    assert_close(ext[toks], oracle_extend(w, tokens=toks, pool=pool), "chunked extend")
+    reqs = _sample_requests(w.decode[0].seq_lens, 5, 6)
+    assert_close(dec[reqs], oracle_decode(w, 0, requests=reqs, pool=pool), "chunked decode")
