@@ -1,0 +1,503 @@
+"""Throughput of the slot-indexed attention hot path on GB300.
+
+One step = one pass of the whole path over one batch: store_kv of every new
+token, extend attention over the chunked-prefill requests, decode attention
+over the decode requests (the chunked-prefill mix workload: 8 extend chunks of
+2,048 tokens after cached prefixes of up to 16,384 tokens, plus 248 decode
+requests with contexts of 1,024..32,768 tokens, Qwen3-0.6B-like GQA 16/8,
+head dim 128, pool of 4,194,304 slots after a 30% leaf-first LRU eviction).
+
+Prints ONE JSON line (rank 0).  `value` is query tokens (extend + decode) per
+second of device time with inputs resident in HBM; `e2e` is the same metric
+with the step's inputs copied from pinned host memory and its outputs read
+back inside the timed region.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from radixattention_prefix_shared_gb300 import workloads as W  # noqa: E402
+from radixattention_prefix_shared_gb300 import workmodel as WM  # noqa: E402
+
+METRIC = "extend+decode attention tokens/s; HBM GB/s and TC util vs GB300 peak"
+WORKLOAD_NAMES = {1: "tiny", 2: "decode_llama7b", 3: "shared_prompt_extend",
+                  4: "tree_of_thought_decode", 5: "chunked_prefill_mix"}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash(name: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("common.cuh", name):
+        with open(os.path.join(ROOT, "radixattention_prefix_shared_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        e = d[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash(e["source_file"]):
+            return None
+        return int(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, group=None, device=None) -> float:
+    """Largest value of x over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- GPU arm
+
+class Step:
+    """Device buffers of one workload and the launches of one step."""
+
+    def __init__(self, w: W.Workload, device):
+        import torch
+        from radixattention_prefix_shared_gb300 import binding as B
+        self.B, self.torch, self.w, self.dev = B, torch, w, device
+        t = W.to_device(w, device)
+        self.t = t
+        d = w.dims
+        self.Hq, self.Hkv, self.D = d.num_q_heads, d.num_kv_heads, d.head_dim
+        # one store_kv over every new token: the extend and first-decode k/v
+        # are views of one contiguous buffer
+        parts_k, parts_v, parts_s = [], [], []
+        if w.extend is not None:
+            parts_k.append(t["extend"]["k_new"]); parts_v.append(t["extend"]["v_new"])
+            parts_s.append(t["extend"]["slots"])
+        if w.decode:
+            parts_k.append(t["decode"][0]["k_new"]); parts_v.append(t["decode"][0]["v_new"])
+            parts_s.append(t["decode"][0]["slots"])
+        self.k_all = torch.cat(parts_k).contiguous()
+        self.v_all = torch.cat(parts_v).contiguous()
+        self.s_all = torch.cat(parts_s).contiguous()
+        n_ext = 0
+        if w.extend is not None:
+            n_ext = w.extend.total_extend
+            t["extend"]["k_new"] = self.k_all[:n_ext]
+            t["extend"]["v_new"] = self.v_all[:n_ext]
+        if w.decode:
+            t["decode"][0]["k_new"] = self.k_all[n_ext:]
+            t["decode"][0]["v_new"] = self.v_all[n_ext:]
+        self.ws_ext = B.new_workspace(256, device)
+        self.out_ext = torch.empty_like(t["extend"]["q"]) if w.extend is not None else None
+        self.out_dec, self.ws_dec = [], []
+        for b, tb in zip(w.decode, t["decode"]):
+            self.out_dec.append(torch.empty_like(tb["q"]))
+            dims = B.make_dims(self.Hq, self.Hkv, self.D, d.pool_size)
+            self.ws_dec.append(B.new_workspace(B.decode_workspace_bytes(b.q.shape[0], int(b.seq_lens.max()), dims), device))
+        self.tokens = (w.extend.total_extend if w.extend is not None else 0) + sum(b.q.shape[0] for b in w.decode)
+        self.launches = 0
+
+    def run(self, ev=None):
+        """One step; records events [start, after store, after extend, after decode]."""
+        B, t, w = self.B, self.t, self.w
+        launches = 0
+        if ev is not None:
+            ev[0].record()
+        B.sgl_store_kv(self.k_all, self.v_all, self.s_all, t["pool_k"], t["pool_v"])
+        launches += 1
+        if ev is not None:
+            ev[1].record()
+        if w.extend is not None:
+            e, te = w.extend, t["extend"]
+            B.sgl_extend_attention(te["q"], te["k_new"], te["v_new"], t["pool_k"], t["pool_v"],
+                                   t["req_to_token"], te["req_pool_idx"], te["prefix_lens"],
+                                   te["extend_lens"], self.out_ext, max_extend=int(e.extend_lens.max()),
+                                   max_prefix=int(e.prefix_lens.max()), workspace=self.ws_ext)
+            launches += 1
+        if ev is not None:
+            ev[2].record()
+        for s, (b, tb) in enumerate(zip(w.decode, t["decode"])):
+            if s > 0:
+                B.sgl_store_kv(tb["k_new"], tb["v_new"], tb["slots"], t["pool_k"], t["pool_v"])
+                launches += 1
+            B.sgl_decode_attention(tb["q"], t["pool_k"], t["pool_v"], t["req_to_token"], tb["req_pool_idx"],
+                                   tb["seq_lens"], self.out_dec[s], max_seq_len=int(b.seq_lens.max()),
+                                   workspace=self.ws_dec[s])
+            launches += 3
+        if ev is not None:
+            ev[3].record()
+        self.launches = launches
+
+    # inputs that arrive from the host every step, and the results read back
+    def host_io(self):
+        import torch
+        ins, outs = [self.k_all, self.v_all, self.s_all], []
+        if self.w.extend is not None:
+            te = self.t["extend"]
+            ins += [te["q"], te["req_pool_idx"], te["prefix_lens"], te["extend_lens"]]
+            outs.append(self.out_ext)
+        for s, tb in enumerate(self.t["decode"]):
+            ins += [tb["q"], tb["req_pool_idx"], tb["seq_lens"]]
+            if s > 0:
+                ins += [tb["k_new"], tb["v_new"], tb["slots"]]
+            outs.append(self.out_dec[s])
+        pin_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in ins]
+        pin_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+        return list(zip(pin_in, ins)), list(zip(outs, pin_out))
+
+
+def work_of(w: W.Workload):
+    d = w.dims
+    flops = 0
+    ext_bytes = 0
+    if w.extend is not None:
+        e = w.extend
+        flops = WM.extend_flops(e.prefix_lens, e.extend_lens, d.num_q_heads, d.head_dim)
+        ext_bytes = WM.extend_bytes(e.prefix_lens, e.extend_lens, d.num_q_heads, d.num_kv_heads, d.head_dim)
+    dec_bytes = sum(WM.decode_bytes(b.seq_lens, d.num_q_heads, d.num_kv_heads, d.head_dim) for b in w.decode)
+    n_new = (w.extend.total_extend if w.extend is not None else 0) + sum(b.q.shape[0] for b in w.decode)
+    st_bytes = WM.store_kv_bytes(n_new, d.num_kv_heads, d.head_dim)
+    return dict(extend_flops=flops, extend_bytes=ext_bytes, decode_bytes=dec_bytes, store_bytes=st_bytes)
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.make(args.config, seed=1000 + args.config + 7919 * rank)
+    step = Step(w, dev)
+    work = work_of(w)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+        flush.zero_()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            step.run(evs[k])
+            launches += step.launches
+            flush.zero_()                       # outside the events: L2 cold for every step
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier()
+    t_step = [evs[k][0].elapsed_time(evs[k][3]) for k in range(args.steps)]
+    t_store = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
+    t_ext = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
+    t_dec = [evs[k][2].elapsed_time(evs[k][3]) for k in range(args.steps)]
+    total_ms = max_over_ranks(sum(t_step), device=dev)
+    ms_per_step = total_ms / args.steps
+    value = world * step.tokens * args.steps / (total_ms / 1e3)
+
+    # end to end: host inputs in, results out, inside the timed region
+    h2d, d2h = step.host_io()
+    h2d_bytes = sum(x.numel() * x.element_size() for x, _ in h2d)
+    d2h_bytes = sum(x.numel() * x.element_size() for x, _ in d2h)
+    e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        for src, dst in h2d:
+            dst.copy_(src, non_blocking=True)
+        step.run()
+        for src, dst in d2h:
+            dst.copy_(src, non_blocking=True)
+        flush.zero_()
+    torch.cuda.synchronize()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e_steps)]
+    for k in range(e_steps):
+        e_ev[k][0].record()
+        for src, dst in h2d:
+            dst.copy_(src, non_blocking=True)
+        step.run()
+        for src, dst in d2h:
+            dst.copy_(src, non_blocking=True)
+        e_ev[k][1].record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ev) / e_steps, device=dev)
+    e2e_value = world * step.tokens / (e_ms / 1e3)
+
+    pk = peaks()
+    ms_ext = statistics.mean(t_ext)
+    ms_dec = statistics.mean(t_dec)
+    ms_store = statistics.mean(t_store)
+    kernels = {}
+    if work["extend_flops"]:
+        tf = work["extend_flops"] / (ms_ext / 1e3) / 1e12
+        kernels["extend"] = {"ms": round(ms_ext, 4), "tflops": round(tf, 2),
+                             "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                             "algorithmic_tflop": round(work["extend_flops"] / 1e12, 4)}
+    if work["decode_bytes"]:
+        gbs = work["decode_bytes"] / (ms_dec / 1e3) / 1e9
+        kernels["decode"] = {"ms": round(ms_dec, 4), "gbs": round(gbs, 1),
+                             "frac_of_hbm_peak": round(gbs / pk["hbm_gbs"], 4),
+                             "algorithmic_gb": round(work["decode_bytes"] / 1e9, 4),
+                             "launches_per_step": 3 * len(w.decode)}
+    gbs_st = work["store_bytes"] / (ms_store / 1e3) / 1e9
+    kernels["store_kv"] = {"ms": round(ms_store, 4), "gbs": round(gbs_st, 1),
+                           "algorithmic_gb": round(work["store_bytes"] / 1e9, 4)}
+    wl = WORKLOAD_NAMES[args.config]
+    if "decode" in kernels and (ms_dec >= ms_ext or "extend" not in kernels):
+        ach = kernels["decode"]["gbs"]
+        roof = {"kernel": "decode (plan + split + combine)", "bound": "hbm", "achieved": ach,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                "traffic": measured_traffic("decode", wl), "peak_source": pk["source"]}
+    else:
+        ach = kernels["extend"]["tflops"]
+        roof = {"kernel": "extend", "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                "traffic": measured_traffic("extend", wl), "peak_source": pk["source"]}
+    d = w.dims
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl, "num_q_heads": d.num_q_heads, "num_kv_heads": d.num_kv_heads,
+                   "head_dim": d.head_dim, "pool_slots": d.pool_size,
+                   "extend_tokens": int(w.extend.total_extend) if w.extend is not None else 0,
+                   "decode_requests": int(sum(b.q.shape[0] for b in w.decode)),
+                   "query_tokens_per_step": int(step.tokens), "parallelism": f"replicas{world}",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_bytes),
+                "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e_ms, 4)},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": clocks.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+_ORACLE_CACHE: dict = {}
+
+def oracle_sample(config: int, seed: int, budget_s: float, min_tokens: int = 4, max_tokens: int = 100000):
+    """Time the fp64 oracle on query tokens drawn uniformly from one step of
+    the workload until ``budget_s`` of CPU time has been spent."""
+    import oracle
+    if config not in _ORACLE_CACHE:
+        w0 = W.make(config)
+        _ORACLE_CACHE[config] = (w0, [w0.pool_view(decode_steps=s + 1) for s in range(max(1, len(w0.decode)))])
+    w, views = _ORACLE_CACHE[config]
+    pool = views[-1]
+    rng = np.random.default_rng(seed)
+    n_ext = w.extend.total_extend if w.extend is not None else 0
+    n_dec = [b.q.shape[0] for b in w.decode]
+    total = n_ext + sum(n_dec)
+    order = rng.permutation(total)
+    done, spent = 0, 0.0
+    t0 = time.perf_counter()
+    for q_idx in order[:max_tokens]:
+        a = time.perf_counter()
+        if q_idx < n_ext:
+            e = w.extend
+            oracle.extend_attention(e.q, e.k_new, e.v_new, pool.k, pool.v, w.req_to_token, e.req_pool_idx,
+                                    e.prefix_lens, e.extend_lens, w.dims.num_kv_heads, w.dims.sm_scale,
+                                    tokens=[int(q_idx)])
+        else:
+            j = int(q_idx - n_ext)
+            s = 0
+            while j >= n_dec[s]:
+                j -= n_dec[s]
+                s += 1
+            b = w.decode[s]
+            pool_s = views[s]
+            oracle.decode_attention(b.q, pool_s.k, pool_s.v, w.req_to_token, b.req_pool_idx, b.seq_lens,
+                                    w.dims.num_kv_heads, w.dims.sm_scale, requests=[j])
+        spent += time.perf_counter() - a
+        done += 1
+        if spent >= budget_s and done >= min_tokens:
+            break
+    return done, spent, time.perf_counter() - t0
+
+
+def cpu_baseline(config: int, budget_s: float = 15.0):
+    """Run the oracle single-threaded in a fresh process (spawned: no GPU
+    context is inherited) and report its tokens/s on the sample."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"d, s, w = bench.oracle_sample({config}, 0, {budget_s}); "
+            f"print(json.dumps({{'tokens': d, 'seconds': s}}))")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=budget_s * 10 + 600)
+        res = json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # pragma: no cover
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "error": str(exc)[:200]}
+    return {"value": round(res["tokens"] / res["seconds"], 4), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{res['tokens']} query tokens drawn uniformly from one step of "
+                      f"{WORKLOAD_NAMES[config]} (fp64 NumPy, 1 thread, {res['seconds']:.1f} s)"}
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle  # noqa: F401
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for k in range(args.warmup):
+        oracle_sample(args.config, 100 + k, per_step / 2, min_tokens=1, max_tokens=2)
+    toks, secs = 0, 0.0
+    for k in range(args.steps):
+        d, s, _ = oracle_sample(args.config, k, per_step, min_tokens=1)
+        toks += d
+        secs += s
+    value = toks / secs
+    cores = 1 if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else len(os.sched_getaffinity(0))
+    line = {"metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAMES[args.config], "parallelism": "cpu"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{toks} query tokens over {args.steps} steps, drawn uniformly from "
+                                       f"one step of {WORKLOAD_NAMES[args.config]}"},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOAD_NAMES))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
