@@ -145,6 +145,41 @@ sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* p
                                 size_t workspace_bytes, const sgl_attn_dims* dims,
                                 sgl_stream_t stream);
 
+/*
+ * sgl_decode_attention_noalloc -- sgl_decode_attention for callers that
+ * cannot allocate device memory.  The paper has no counterpart: this is a
+ * deployment variant of the decode entry point above.
+ *
+ * Some callers may not call cudaMalloc (or any allocating routine) while they
+ * run attention -- runtimes whose memory planner fixes every device buffer at
+ * start-up, and plugin-style hosts that pass a kernel only its inputs and
+ * outputs -- so they cannot provide the decode workspace.  This call computes
+ * exactly what sgl_decode_attention computes, with the same arguments minus
+ * the workspace, and takes its split-KV scratch from a fixed array of
+ * SGL_DECODE_NOALLOC_SCRATCH_BYTES in the library's own device memory.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - Every GPU that loads the library's module holds the array until the
+ *     process exits.
+ *   - Work whose scratch need (sgl_decode_workspace_bytes(batch, max_seq_len,
+ *     dims)) exceeds SGL_DECODE_NOALLOC_SCRATCH_BYTES is rejected with
+ *     SGL_ERR_WORKSPACE before anything is launched; use sgl_decode_attention
+ *     with a caller workspace for it.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (it must be the current device); make that first call before any
+ *     stream capture.
+ *   - All calls share the array and it keeps the last call's contents:
+ *     calls whose kernels overlap on the GPU race and must be serialised by
+ *     the caller (one stream, or explicit ordering).  No part of it needs
+ *     clearing between calls.
+ */
+#define SGL_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+sgl_status sgl_decode_attention_noalloc(const void* q, const void* pool_k, const void* pool_v,
+                                        const int32_t* req_to_token, int32_t rtt_rows,
+                                        int32_t rtt_stride, const int32_t* req_pool_idx,
+                                        const int32_t* seq_lens, int32_t batch,
+                                        int32_t max_seq_len, void* out, const sgl_attn_dims* dims,
+                                        sgl_stream_t stream);
+
 /* Workspace sizes (host only; no device call). */
 size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims);
 size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_attn_dims* dims);

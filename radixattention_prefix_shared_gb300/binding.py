@@ -41,6 +41,8 @@ _SIGS = {
                                             _P(sgl_attn_dims), c_vp]),
     "sgl_decode_attention": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_i32,
                                             c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims), c_vp]),
+    "sgl_decode_attention_noalloc": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_i32,
+                                                    c_i32, c_vp, _P(sgl_attn_dims), c_vp]),
     "sgl_extend_workspace_bytes": (c_size, [c_i32, c_i32, _P(sgl_attn_dims)]),
     "sgl_decode_workspace_bytes": (c_size, [c_i32, c_i32, _P(sgl_attn_dims)]),
     "sgl_check_store_kv_indices": (ctypes.c_int, [c_vp, c_i32, c_i64, c_vp, c_size, c_vp, c_vp]),
