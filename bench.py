@@ -250,6 +250,16 @@ class Step:
         return list(zip(pin_in, ins)), list(zip(outs, pin_out))
 
 
+# reduced instances of the workloads for profiler captures (a few GB on the
+# device, inputs still larger than L2); same kernels, same per-request shapes
+SMALL = {2: dict(pool_size=1 << 19), 3: dict(pool_size=1 << 17),
+         4: dict(pool_size=1 << 18), 5: dict(pool_size=1 << 19, n_decode=24)}
+
+
+def small_kwargs(args):
+    return SMALL.get(args.config, {}) if getattr(args, "small", False) else {}
+
+
 def work_of(w: W.Workload):
     d = w.dims
     flops = 0
@@ -272,7 +282,7 @@ def gpu_arm(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.make(args.config, seed=1000 + args.config + 7919 * rank)
+    w = W.make(args.config, seed=1000 + args.config + 7919 * rank, **small_kwargs(args))
     step = Step(w, dev)
     work = work_of(w)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
@@ -367,7 +377,7 @@ def gpu_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl, "num_q_heads": d.num_q_heads, "num_kv_heads": d.num_kv_heads,
+        "config": {"workload": wl + ("(small)" if args.small else ""), "num_q_heads": d.num_q_heads, "num_kv_heads": d.num_kv_heads,
                    "head_dim": d.head_dim, "pool_slots": d.pool_size,
                    "extend_tokens": int(w.extend.total_extend) if w.extend is not None else 0,
                    "decode_requests": int(sum(b.q.shape[0] for b in w.decode)),
@@ -490,6 +500,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOAD_NAMES))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="reduced pool / batch of the workload, for profiler captures")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
