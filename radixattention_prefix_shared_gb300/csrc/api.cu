@@ -213,6 +213,7 @@ sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_
   a.batch = batch;
   a.total_extend = total_extend;
   a.max_extend = max_extend;
+  a.pool_size = dims->pool_size;
   a.out = out;
   a.workspace = workspace;
   a.num_q_heads = dims->num_q_heads;

@@ -42,6 +42,43 @@ SGL_DEV float ex2(float x) {
   return y;
 }
 
+// Packed fp32 pair arithmetic: the sm_100-family FFMA2/FADD2 instructions
+// through CUDA's float2 builtins, so register pairs are allocated by the
+// compiler rather than assembled with moves.
+SGL_DEV float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+SGL_DEV float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+SGL_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for two values on the FMA/ALU pipes (no MUFU), by range reduction and a
+// polynomial: x = j + f with j = round(x) read from the low mantissa bits of
+// x + 1.5*2^23 and |f| <= 1/2; 2^f = 1 + f*(c1 + f*(c2 + f*c3)), the cubic
+// fitted by exp2_fit.py (minimax relative error 1.01e-4 on [-1/2, 1/2]);
+// 2^j is added to the exponent field.  x is clamped below at -125, so a
+// masked score (-inf) gives 2^-125 instead of 0 -- negligible next to the
+// unmasked weights of the same row, which include a 1.
+constexpr float kExp2C1 = 0.6932829022407532f;
+constexpr float kExp2C2 = 0.2422109693288803f;
+constexpr float kExp2C3 = 0.055009059607982635f;
+constexpr float kExp2Magic = 12582912.0f;  // 1.5 * 2^23
+SGL_DEV float2 exp2_fma2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 magic = make_float2(kExp2Magic, kExp2Magic);
+  const float2 t = fadd2(x, magic);                                   // round(x) in low bits
+  const float2 j = fadd2(t, make_float2(-kExp2Magic, -kExp2Magic));  // round(x)
+  const float2 f = fadd2(x, make_float2(-j.x, -j.y));                 // |f| <= 1/2
+  float2 q = ffma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
+  q = ffma2(q, f, make_float2(kExp2C1, kExp2C1));
+  q = ffma2(q, f, make_float2(1.f, 1.f));
+  const int mb = __float_as_int(kExp2Magic);
+  return make_float2(__int_as_float(__float_as_int(q.x) + ((__float_as_int(t.x) - mb) << 23)),
+                     __int_as_float(__float_as_int(q.y) + ((__float_as_int(t.y) - mb) << 23)));
+}
+
 // Unpack 8 bf16 held in a uint4 into 8 floats (a bf16 is the top half of a float).
 SGL_DEV void bf16x8_to_f32(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -73,8 +110,16 @@ SGL_DEV void cp_async_wait() {
 }
 SGL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Make this thread's generic-proxy shared-memory writes (cp.async included)
-// visible to later async-proxy reads (tcgen05.mma operands).
+// Arrive on `bar` once every cp.async issued so far by this thread has
+// completed (the arrival is pre-counted in the barrier's expected count).
+SGL_DEV void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Order generic-proxy shared-memory writes (cp.async included) that this
+// thread has observed before its later async-proxy accesses (tcgen05.mma
+// operand reads).
 SGL_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -94,36 +139,105 @@ SGL_DEV void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
-SGL_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One bounded probe of the phase: the thread may sleep in hardware until the
+// phase completes or about `hint_ns` elapse, so waiting warps do not spin.
+SGL_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 100000u) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall time or as soon as another thread raised *abort; on a
-// timeout it raises *abort and records kDevWaitTimeout in *status.  Returns
-// false when it gave up.
+// `limit_ns` of wall time or as soon as another thread raised *abort (when
+// `abort` is given); on a timeout it raises *abort and records
+// kDevWaitTimeout in *status (when given).  Returns false when it gave up.
 SGL_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                                uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
+    if ((it & 7u) == 0) {
+      if (abort && *abort) return false;
       if (global_timer_ns() - t0 > limit_ns) {
-        *abort = 1;
+        if (abort) *abort = 1;
         if (status) atomicExch(status, (int)kDevWaitTimeout);
         return false;
       }
     }
   }
+}
+
+SGL_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// ----------------------------------------------------------------- TMA
+
+// Tiled tensor loads into shared memory, completion counted in bytes on `bar`.
+SGL_DEV void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+SGL_DEV void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+// Four rows y0..y3 (one box-width each, starting at column x) of a 2-D tensor
+// into four consecutive 128-byte rows of shared memory.
+SGL_DEV void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t y0, int32_t y1,
+                         int32_t y2, int32_t y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+SGL_DEV void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ----------------------------------------------------------------- named barriers
+
+SGL_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier over `nthreads` threads that also returns the OR of `pred` over them.
+SGL_DEV bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, %3, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+// Barrier over `nthreads` threads that returns how many of them had `pred` set.
+SGL_DEV uint32_t bar_red_popc(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred pi;\n setp.ne.u32 pi, %1, 0;\n bar.red.popc.u32 %0, %2, %3, pi;\n}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return out;
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -225,6 +339,15 @@ SGL_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
           taddr),
       SGL_W32(r)
+      : "memory");
+}
+SGL_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
       : "memory");
 }
 SGL_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

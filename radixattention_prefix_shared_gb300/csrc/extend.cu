@@ -16,19 +16,27 @@
 // and walks the KV blocks (128 keys each): first the prefix blocks (rows
 // gathered from the pool), then the suffix blocks (rows of k_new/v_new).
 //
-// Warp roles (11 warps):
-//   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127)
-//   warps 4-7  softmax for Q tile 1
-//   warps 8-9  producers: 16-byte cp.async gathers of Q, K and V rows into
-//              the 128-byte-swizzled shared-memory layout the tensor core reads
-//   warp 10    TMEM allocation and the single thread that issues tcgen05.mma
+// Warp roles (19 warps):
+//   warps 0-15 softmax: Q tile t = (w/4)%2, TMEM lane quarter w%4, key-column
+//              half w/8 -- two warps share the rows of a lane quarter, each
+//              taking 64 of the block's 128 keys
+//   warps 16-17 producers: 16-byte cp.async gathers of Q, K and V rows into
+//              the 128-byte-swizzled shared-memory layout the tensor core
+//              reads; each thread's arrival on the stage's mbarrier fires in
+//              hardware when its copies land (cp.async.mbarrier.arrive), so a
+//              producer never waits for its own copies; the MMA thread orders
+//              the landed data for the tensor core with a proxy fence
+//   warp 18    TMEM allocation and the single thread that issues tcgen05.mma
 // TMEM (512 columns): S0 | S1 | O0 | O1.  S_t = Q_t K^T lands in TMEM as
 // fp32; the softmax warps read it, write P = exp2(S*scale*log2e - m) as
 // bf16 over the first half of S_t's columns, and O_t += P V is issued with A
 // read from TMEM.  The two Q tiles ping-pong: while softmax works on one
-// tile the tensor core computes the other.  The running max is only moved
-// when a block's max exceeds it by more than 2^8 (O is then rescaled in
-// TMEM), so most blocks need no correction pass.
+// tile the tensor core computes the other.  The reference max used for the
+// exponentials lags the running max lazily: a block is accepted while its
+// row sum stays <= 2^32 (every weight then fits fp32 and bf16 with full
+// relative precision); otherwise the block max becomes the reference and O
+// is rescaled in TMEM, so most blocks need neither a max pass nor a
+// correction pass.
 //
 // Every wait on an mbarrier is bounded (2 s); on a timeout the kernel raises
 // an abort flag, records a status word in the workspace, drains its own
@@ -42,21 +50,25 @@ namespace {
 
 constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per KV block
-constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxWarps = 16;
 constexpr int kProducerWarps = 2;
-constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;  // 10
-constexpr int kThreads = (kMmaWarp + 1) * 32;              // 352
+constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;  // 18
+constexpr int kThreads = (kMmaWarp + 1) * 32;              // 608
 constexpr int kProducerThreads = kProducerWarps * 32;
 // a producer thread copies 16-byte chunk (ptid % 8) of rows
 // ptid / 8 + kRowStep * i, i < kRowsPerThread, of every 128-row tile
 constexpr int kRowStep = kProducerThreads / 8;
 constexpr int kRowsPerThread = 128 / kRowStep;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kAcceptSum = 4294967296.0f;  // 2^32: largest accepted block row sum
 constexpr uint32_t kTmemCols = 512;
 // TMEM column of S_t and O_t
 SGL_DEV constexpr uint32_t col_s(int t) { return 128u * t; }
 SGL_DEV constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
-constexpr int kLag = 2;  // cp.async groups a producer keeps in flight before publishing
+#ifndef SGL_FMA_EXP_PAIRS_PER8
+#define SGL_FMA_EXP_PAIRS_PER8 0
+#endif
+// of every 8 score pairs, this many are exponentiated on the FMA pipe
+constexpr int kFmaExpPairsPer8 = SGL_FMA_EXP_PAIRS_PER8;
 
 template <int D>
 struct Cfg {
@@ -64,7 +76,6 @@ struct Cfg {
   static constexpr int kChunkBytes = 128 * 128;     // 128 rows x 128 bytes
   static constexpr int kTileBytes = 128 * D * 2;    // Q tile or one K / V block
   static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots
-  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024 + 1024;
 };
 
 struct Bars {
@@ -78,7 +89,16 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
   int32_t red[32];
+  float xchg[2][2][128];  // [tile][column half][row]: block maxima, final row sums
 };
+
+// dynamic shared memory: 1024 bytes of alignment slack, Q tiles, the K/V ring, barriers
+template <int D>
+constexpr int smem_bytes() {
+  return 1024 + (2 + Cfg<D>::kStages) * Cfg<D>::kTileBytes + (int)sizeof(Bars);
+}
+static_assert(smem_bytes<128>() <= 227 * 1024, "extend kernel shared memory");
+static_assert(smem_bytes<64>() <= 227 * 1024, "extend kernel shared memory");
 
 struct Params {
   const __nv_bfloat16* q;
@@ -140,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
     mbar_init(&bars->q_full, kProducerThreads);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_ready[t], 128);
+      mbar_init(&bars->p_ready[t], 8 * 32);  // the 8 softmax warps of the tile
     }
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
@@ -166,73 +186,114 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
 
   if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    // warp w: Q tile t, key-column half h, TMEM lane quarter q (rows 32q..)
+    const int t = (warp >> 2) & 1, h = warp >> 3, q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t tS = tmem + lane_off + col_s(t);
     const uint32_t tO = tmem + lane_off + col_o(t);
+    const uint32_t pair_bar = 1 + t * 4 + q;  // named barrier of the two halves of these rows
+    float* xchg_mine = &bars->xchg[t][h][row];
+    const float* xchg_other = &bars->xchg[t][h ^ 1][row];
     const int tok = q0 + t * p.tpt + row / p.g;
     const bool row_valid = row < p.rows_used && tok < e;
     const int tok_i = row_valid ? tok : (1 << 30);  // padding rows see every key
-    float m_ref = -INFINITY, l = 0.f;
+    const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+    float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     bool ok = true;
     for (int b = 0; b < nb && ok; ++b) {
-      ok = warp_wait(&bars->s_full[t], b & 1, bars, p.status);
-      if (!ok) break;
+      const bool ok_w = warp_wait(&bars->s_full[t], b & 1, bars, p.status);
       tc_fence_after();
-      uint32_t sr[BN];
-#pragma unroll
-      for (int j = 0; j < BN / 32; ++j)
-        tmem_ld32(tS + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * j]));
-      tmem_wait_ld();
-      // visible keys of this block: c < limit
+      // visible keys of this block: c < limit (key index within the block)
       int limit;
       if (b < nb_pre) limit = pfx - b * BN;
       else limit = tok_i - (b - nb_pre) * BN + 1;
-      limit = max(0, min(BN, limit));
-      float mx = -INFINITY;
+      limit = max(0, min(BN, limit)) - 64 * h;  // relative to this half's first key
+      uint32_t sr[64];
+      auto load_s = [&]() {
+        tmem_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_wait_ld();
+        if (limit < 64) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float v = c < limit ? __uint_as_float(sr[c]) : -INFINITY;
-        sr[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
-      }
-      const float mx2 = mx * p.scale_log2;
-      const bool need = mx2 > m_ref + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx2);
-        m_ref = mx2;
-      }
-      l *= alpha;
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        // keys 64*half .. 64*half+63 -> 32 packed bf16 pairs -> TMEM columns 32*half..
-        uint32_t pk[32];
+          for (int c = 0; c < 64; ++c)
+            if (c >= limit) sr[c] = __float_as_uint(-INFINITY);
+        }
+      };
+      // P of this half's 64 keys against reference m_use, packed as bf16
+      // pairs in place over sr[0..31]; returns the half's row sum
+      auto make_p = [&](float m_use) {
+        const float2 nm = make_float2(-m_use, -m_use);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const int k = 64 * half + 2 * c;
-          const float p0 = ex2(fmaf(__uint_as_float(sr[k]), p.scale_log2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[k + 1]), p.scale_log2, -m_use));
-          sum += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+          const float2 x =
+              ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc, nm);
+          float2 pw;
+          if ((c & 7) >= 8 - kFmaExpPairsPer8) {
+            pw = exp2_fma2(x);
+          } else {
+            pw = make_float2(ex2(x.x), ex2(x.y));
+          }
+          if (c & 1) acc1 = fadd2(acc1, pw);
+          else acc0 = fadd2(acc0, pw);
+          sr[c] = pack_bf16x2(pw.x, pw.y);
         }
-        tmem_st32(tS + 32 * half, pk);
+        return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      };
+      float psum = 0.f;
+      bool need = false;
+      // (after a failed wait this reads stale columns of the CTA's own TMEM;
+      // the vote below then ends the loop for both halves)
+      load_s();
+      if (b > 0) {
+        // lazy reference: accept the block while this half's row sum stays
+        // <= 2^32 (every weight <= 2^32, safe in fp32 and bf16)
+        psum = make_p(m_ref);
+        need = !(psum <= kAcceptSum);
       }
-      l += sum;
-      if (b > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds blocks < b (PV of block b-1 completed before S of block b
-        // was committed); bring it to the new reference max
+      // The two halves of these rows vote together (one barrier): lane 0 votes
+      // "a row of this warp broke the bound", lanes 1-4 vote "this warp gave
+      // up waiting".  Both halves then leave together or recompute together
+      // (any row over the bound, or the first block, moves the pair to the
+      // block max).  The barrier also orders both halves' S reads before
+      // either writes P over S's first 64 columns.
+      const bool need_w = __any_sync(0xffffffffu, need);
+      const uint32_t votes =
+          bar_red_popc(pair_bar, 64, (lane == 0 && need_w) || (lane >= 1 && lane <= 4 && !ok_w));
+      if (votes >= 4) {
+        ok = false;
+        break;
+      }
+      const bool redo = (b == 0) || (votes & 3) != 0;
+      float alpha = 1.f;
+      if (redo) {
+        if (b > 0) load_s();  // P overwrote the registers; S is still in TMEM
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
+        for (int c = 0; c < 64; c += 2)
+          mq[(c >> 1) & 3] = fmax3(mq[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        *xchg_mine = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        named_bar_sync(pair_bar, 64);
+        const float mx2 = fmaxf(*xchg_mine, *xchg_other) * p.scale_log2;
+        named_bar_sync(pair_bar, 64);  // both read before the buffer is reused
+        const float m_new = fmaxf(m_ref, mx2);
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+        m_ref = m_new;
+        psum = make_p(m_ref == -INFINITY ? 0.f : m_ref);
+      }
+      tmem_st32(tS + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      l = l * alpha + psum;
+      if (b > 0 && redo) {
+        // O (this half's D/2 columns) holds blocks < b: bring it to the new reference
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) {
           uint32_t o[32];
-          tmem_ld32(tO + 32 * j, o);
+          tmem_ld32(tO + (D / 2) * h + 32 * j, o);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(tO + 32 * j, o);
+          tmem_st32(tO + (D / 2) * h + 32 * j, o);
         }
       }
       tmem_wait_st();
@@ -240,15 +301,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
       mbar_arrive(&bars->p_ready[t]);
     }
     if (ok) ok = warp_wait(&bars->o_done, 0, bars, p.status);
+    // every softmax warp reaches this barrier exactly once (ok or not)
+    *xchg_mine = l;
+    named_bar_sync(pair_bar, 64);
+    const float lrow = *xchg_mine + *xchg_other;
     if (ok) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      // this half writes columns [h*D/2, (h+1)*D/2) of the output row
       __nv_bfloat16* orow =
-          p.out + ((int64_t)(off + tok) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D;
+          p.out + ((int64_t)(off + tok) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + (D / 2) * h;
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
+      for (int j = 0; j < D / 64; ++j) {
         uint32_t o[32];
-        tmem_ld32(tO + 32 * j, o);
+        tmem_ld32(tO + (D / 2) * h + 32 * j, o);
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
@@ -283,14 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
                       valid ? src + c * 64 : p.q, valid ? 16u : 0u);
       }
     }
-    cp_async_commit();
-    int issued = 1, published = 0;
-    auto publish_oldest = [&]() {
-      fence_proxy_async_smem();
-      if (published == 0) mbar_arrive(&bars->q_full);
-      else mbar_arrive(&bars->kv_full[(published - 1) % C::kStages]);
-      ++published;
-    };
+    // each producer thread's arrival on q_full / kv_full fires when its own
+    // copies have landed (no producer ever waits for its copies)
+    cp_async_mbar_arrive(&bars->q_full);
     const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride;
     int32_t slot_cur[kRowsPerThread], slot_next[kRowsPerThread];
     auto load_slots = [&](int b, int32_t (&dst)[kRowsPerThread]) {
@@ -312,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
       if (!is_v) {
 #pragma unroll
         for (int i = 0; i < kRowsPerThread; ++i) slot_cur[i] = slot_next[i];
+        if (b + 1 < nb_pre) load_slots(b + 1, slot_next);
       }
       const uint32_t dst0 = sKV_a + stage * C::kTileBytes;
       if (b < nb_pre) {
@@ -341,18 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
             cp_async_16(dst0 + c * C::kChunkBytes + sw128(row, ci), src + c * 64, valid ? 16u : 0u);
         }
       }
-      cp_async_commit();
-      ++issued;
-      if (is_v && b + 1 < nb_pre) load_slots(b + 1, slot_next);
-      if (issued - published > kLag) {
-        cp_async_wait<kLag>();
-        publish_oldest();
-      }
+      cp_async_mbar_arrive(&bars->kv_full[stage]);
     }
-    cp_async_wait_all();
-    if (ok)
-      while (published < issued) publish_oldest();
-  } else if (lane == 0) {
+    cp_async_wait_all();  // nothing of this CTA's shared memory is still being written
+  } else if (warp == kMmaWarp && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idS = make_idesc_bf16(BM, BN, false);
     constexpr uint32_t idO = make_idesc_bf16(BM, D, true);
@@ -376,11 +430,17 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
         umma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bd, idO, (acc || kk > 0) ? 1u : 0u);
       }
     };
+    // copies landed by cp.async (generic proxy) are read by the tensor core
+    // (async proxy): order them with a proxy fence after each wait
     bool ok = wait(&bars->q_full, 0);
-    if (ok) tc_fence_after();
+    if (ok) {
+      fence_proxy_async_smem();
+      tc_fence_after();
+    }
     for (int b = 0; b < nb && ok; ++b) {
       const int kt = 2 * b, ks = kt % C::kStages;
       if (!(ok = wait(&bars->kv_full[ks], (kt / C::kStages) & 1))) break;
+      fence_proxy_async_smem();
       tc_fence_after();
       int vt = 0, vs = 0;
       if (b > 0) {
@@ -388,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
         vs = vt % C::kStages;
         if (!(ok = wait(&bars->p_ready[0], (b - 1) & 1))) break;
         if (!(ok = wait(&bars->kv_full[vs], (vt / C::kStages) & 1))) break;
+        fence_proxy_async_smem();
         tc_fence_after();
         issue_pv(0, vs, b > 1);
       }
@@ -407,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
       const int vt = 2 * nb - 1, vs = vt % C::kStages;
       ok = wait(&bars->p_ready[0], (nb - 1) & 1) && wait(&bars->kv_full[vs], (vt / C::kStages) & 1);
       if (ok) {
+        fence_proxy_async_smem();
         tc_fence_after();
         issue_pv(0, vs, nb > 1);
         ok = wait(&bars->p_ready[1], (nb - 1) & 1);
@@ -421,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
     if (!ok) {
       // let every MMA issued so far finish before TMEM is released
       umma_commit(&bars->drain);
-      mbar_wait_bounded(&bars->drain, 0, &bars->abort, nullptr, 2000000000ull);
+      mbar_wait_bounded(&bars->drain, 0, nullptr, nullptr);
     }
   }
   tc_fence_before();
@@ -436,13 +498,13 @@ template <int D>
 sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = extend_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<D>()) !=
       cudaSuccess)
     return SGL_ERR_CUDA;
   const int per_cta = 2 * prm.tpt;
   const unsigned gx = (unsigned)((max_extend + per_cta - 1) / per_cta);
   dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)batch);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(prm);
+  kern<<<grid, kThreads, smem_bytes<D>(), stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
 }
 

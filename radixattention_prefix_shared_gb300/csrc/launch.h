@@ -46,6 +46,7 @@ struct ExtendArgs {
   const int32_t* prefix_lens;
   const int32_t* extend_lens;
   int32_t batch, total_extend, max_extend;
+  int64_t pool_size;
   void* out;
   void* workspace;
   int32_t num_q_heads, num_kv_heads, head_dim;

@@ -250,3 +250,30 @@ def test_zero_sized_calls_are_noops():
                            max_seq_len=1)
     B.sgl_extend_attention(z, z, z, pool, pool, rtt, i0, i0, i0, max_extend=0)
     torch.cuda.synchronize()
+
+
+def test_repeated_launches_are_bit_identical():
+    """The kernels are deterministic: repeated launches over the same inputs
+    (many K/V ring reuses per CTA) give identical bits, and they match the
+    oracle -- any read of a shared-memory stage before its copies landed would
+    show up as a run-to-run difference."""
+    w = extend_case(61, Hq=16, Hkv=8, D=128, prefix_lens=[3000, 1700, 40], extend_lens=[300, 129, 700],
+                    decode_after=True)
+    run = Run(w)
+    first = run.extend()
+    assert_close(first, oracle_extend(w), "repeated extend")
+    e, te = w.extend, run.t["extend"]
+    for _ in range(12):
+        out = B.sgl_extend_attention(te["q"], te["k_new"], te["v_new"], run.t["pool_k"], run.t["pool_v"],
+                                     run.t["req_to_token"], te["req_pool_idx"], te["prefix_lens"],
+                                     te["extend_lens"], max_extend=int(e.extend_lens.max()),
+                                     max_prefix=int(e.prefix_lens.max()), workspace=run.ws_ext)
+        torch.cuda.synchronize()
+        assert np.array_equal(W.bf16_bits(out), first)
+    d0 = run.decode()
+    b, tb = w.decode[0], run.t["decode"][0]
+    for _ in range(4):
+        out = B.sgl_decode_attention(tb["q"], run.t["pool_k"], run.t["pool_v"], run.t["req_to_token"],
+                                     tb["req_pool_idx"], tb["seq_lens"], max_seq_len=int(b.seq_lens.max()))
+        torch.cuda.synchronize()
+        assert np.array_equal(W.bf16_bits(out), d0)
