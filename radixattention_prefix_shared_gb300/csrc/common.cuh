@@ -173,45 +173,6 @@ SGL_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abo
   }
 }
 
-SGL_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// ----------------------------------------------------------------- TMA
-
-// Tiled tensor loads into shared memory, completion counted in bytes on `bar`.
-SGL_DEV void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-SGL_DEV void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
-                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-// Four rows y0..y3 (one box-width each, starting at column x) of a 2-D tensor
-// into four consecutive 128-byte rows of shared memory.
-SGL_DEV void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t y0, int32_t y1,
-                         int32_t y2, int32_t y3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-SGL_DEV void tma_prefetch_desc(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
-}
-
 // ----------------------------------------------------------------- named barriers
 
 SGL_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
