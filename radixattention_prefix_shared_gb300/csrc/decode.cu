@@ -31,9 +31,18 @@ namespace sgl {
 
 namespace {
 
-constexpr int kChunk = 512;  // keys per work item
-constexpr int kTile = 32;    // keys per pipeline stage
-constexpr int kStages = 4;   // ring depth
+#ifndef SGL_DECODE_CHUNK
+#define SGL_DECODE_CHUNK 512
+#endif
+#ifndef SGL_DECODE_TILE
+#define SGL_DECODE_TILE 32
+#endif
+#ifndef SGL_DECODE_STAGES
+#define SGL_DECODE_STAGES 4
+#endif
+constexpr int kChunk = SGL_DECODE_CHUNK;  // keys per work item
+constexpr int kTile = SGL_DECODE_TILE;    // keys per pipeline stage
+constexpr int kStages = SGL_DECODE_STAGES;  // ring depth
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
