@@ -7,9 +7,11 @@
 // values from wherever they sit in the pool.
 //
 // Schedule (split-KV):
-//   1. plan    -- one block lists the work items (request, split), a split
-//                 being up to kChunk consecutive keys of one request;
-//   2. split   -- a persistent grid (x: work items, strided; y: KV head) runs
+//   1. plan    -- one block lists the work items (request, split): a
+//                 request's keys are cut into ceil(seq_len / kChunk) runs of
+//                 near-equal length;
+//   2. split   -- a persistent grid (x: two waves of CTAs taking items from a
+//                 per-KV-head counter; y: KV head) runs
 //                 each item: the slot indices go to shared memory, K and V
 //                 rows of the KV head are gathered by 16-byte cp.async into a
 //                 kStages-deep ring of kTile-key tiles, and the query heads of
@@ -51,6 +53,7 @@ struct Ws {
   int32_t* item_start;  // [B+1]
   int2* items;          // [max_items]
   int32_t* n_items;     // [1]
+  int32_t* next_item;   // [Hkv] work counters (zeroed by the plan kernel)
   float2* part_ml;      // [max_items, Hkv, G]  (max in log2 units, sum)
   float* part_acc;      // [max_items, Hkv, G, D]
 };
@@ -70,6 +73,8 @@ inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G
   off = align256(off + sizeof(int2) * (size_t)max_items);
   size_t o_n = off;
   off = align256(off + sizeof(int32_t));
+  size_t o_next = off;
+  off = align256(off + sizeof(int32_t) * (size_t)Hkv);
   size_t o_ml = off;
   off = align256(off + sizeof(float2) * (size_t)max_items * Hkv * G);
   size_t o_acc = off;
@@ -79,6 +84,7 @@ inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G
     ws->item_start = reinterpret_cast<int32_t*>(b + o_start);
     ws->items = reinterpret_cast<int2*>(b + o_items);
     ws->n_items = reinterpret_cast<int32_t*>(b + o_n);
+    ws->next_item = reinterpret_cast<int32_t*>(b + o_next);
     ws->part_ml = reinterpret_cast<float2*>(b + o_ml);
     ws->part_acc = reinterpret_cast<float*>(b + o_acc);
   }
@@ -103,9 +109,10 @@ struct Params {
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ seq_lens,
                                                            int32_t batch, int64_t max_items,
-                                                           Ws ws) {
+                                                           int32_t Hkv, Ws ws) {
   __shared__ int32_t warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int h = tid; h < Hkv; h += blockDim.x) ws.next_item[h] = 0;
   const int per = (batch + blockDim.x - 1) / blockDim.x;
   const int r0 = min(batch, tid * per), r1 = min(batch, r0 + per);
   int32_t local = 0;
@@ -178,12 +185,24 @@ decode_split_kernel(Params p) {
   const int kvh = blockIdx.y;
   const int32_t n_items = *p.ws.n_items;
   const uint32_t ring = smem_u32(smem);
+  // items are taken dynamically from the KV head's counter; the next index
+  // is fetched while the current item runs
+  __shared__ int32_t s_item[2];
+  if (tid == 0) s_item[0] = atomicAdd(&p.ws.next_item[kvh], 1);
+  __syncthreads();
+  int buf = 0;
 
-  for (int32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+  for (int32_t item = s_item[0]; item < n_items; item = s_item[buf]) {
+    int32_t next = 0;
+    if (tid == 0) next = atomicAdd(&p.ws.next_item[kvh], 1);
     const int2 it = p.ws.items[item];
     const int r = it.x;
-    const int32_t t0 = it.y * kChunk;
-    const int32_t n = min(p.seq_lens[r] - t0, kChunk);
+    // the request's keys are cut into ceil(seq / kChunk) near-equal items
+    const int32_t seq = p.seq_lens[r];
+    const int32_t ns = (seq + kChunk - 1) / kChunk;
+    const int32_t base = seq / ns, rem = seq % ns;
+    const int32_t t0 = it.y * base + min(it.y, rem);
+    const int32_t n = base + (it.y < rem ? 1 : 0);
     const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride + t0;
     for (int i = tid; i < n; i += kThreads) s_slots[i] = rtt[i];
 
@@ -359,7 +378,9 @@ decode_split_kernel(Params p) {
         if (d == 0) p.ws.part_ml[slot] = make_float2(M, Ls);
       }
     }
-    __syncthreads();  // scratch and slots are rewritten by the next item
+    if (tid == 0) s_item[buf ^ 1] = next;
+    buf ^= 1;
+    __syncthreads();  // scratch, slots and the next item index
   }
 }
 
@@ -411,12 +432,13 @@ sgl_status run(const Params& prm, int64_t max_items, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SGL_ERR_CUDA;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.ws);
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.Hkv, prm.ws);
   int blocks_per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, kThreads, smem) !=
           cudaSuccess ||
       blocks_per_sm < 1)
     blocks_per_sm = 1;
+  // two waves of CTAs (every CTA keeps taking items while any are left)
   int64_t gx = ((int64_t)2 * blocks_per_sm * num_sms() + prm.Hkv - 1) / prm.Hkv;
   if (gx > max_items) gx = max_items;
   if (gx < 1) gx = 1;
