@@ -277,7 +277,7 @@ class Step:
 
 # reduced instances of the workloads for profiler captures (a few GB on the
 # device, inputs still larger than L2); same kernels, same per-request shapes
-SMALL = {2: dict(pool_size=1 << 19), 3: dict(pool_size=1 << 17),
+SMALL = {2: dict(pool_size=1 << 18), 3: dict(pool_size=1 << 17),
          4: dict(pool_size=1 << 18), 5: dict(pool_size=1 << 19, n_decode=24)}
 
 
@@ -457,7 +457,8 @@ def oracle_sample(config: int, seed: int, budget_s: float, min_tokens: int = 4, 
     import oracle
     if config not in _ORACLE_CACHE:
         w0 = W.make(config)
-        _ORACLE_CACHE[config] = (w0, [w0.pool_view(decode_steps=s + 1) for s in range(max(1, len(w0.decode)))])
+        views = [w0.pool_view(decode_steps=s + 1) for s in range(len(w0.decode))] or [w0.pool_view()]
+        _ORACLE_CACHE[config] = (w0, views)
     w, views = _ORACLE_CACHE[config]
     pool = views[-1]
     rng = np.random.default_rng(seed)

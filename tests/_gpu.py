@@ -21,6 +21,8 @@ def assert_close(got_bits, want, what=""):
     err = np.abs(got - want)
     assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3g}"
     assert err.mean() <= MEAN_ABS, f"{what}: mean abs err {err.mean():.3g}"
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    print(f"\n[parity] {what}: max abs {err.max():.3e} mean abs {err.mean():.3e} output rms {rms:.3e}")
     return err.max(), err.mean()
 
 
