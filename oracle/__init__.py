@@ -18,6 +18,11 @@ What it computes, and where the pages fix it:
     computed (EXTEND) -- "Origins", Batching: Req, Batch and the three forward
     modes; Execution (extend_attention_fwd reads k and v from the pool through
     req_to_token).
+  * cascade decode: the same decode output assembled from per-group softmax
+    states (keys shared by several requests, read once per group) and each
+    request's private tail, merged exactly; shared prefixes are identical
+    slot numbers in the rows ("Inside SGLang", Step 3: Paged KV and the
+    kernels that read it).
 All arithmetic is float64.  Every function is pinned by ``tests/test_oracle.py``
 against closed forms, a library routine (full causal attention recomputed from
 scratch), invariants and brute force; see that file for the list.
@@ -30,4 +35,7 @@ from .attention import (  # noqa: F401
     request_kv,
     extend_attention,
     decode_attention,
+    partial_state,
+    merge_states,
+    cascade_decode_attention,
 )

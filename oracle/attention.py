@@ -140,3 +140,82 @@ def decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_lens,
             kh = _kv_head_of(h, Hq, num_kv_heads)
             out[n, h] = _softmax_attend(qr[h], K[:, kh], V[:, kh], scale)
     return out
+
+
+# ---------------------------------------------------------------- cascade
+
+def partial_state(qv: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """Softmax state of one query over a subset of its keys, float64:
+    ``(m, l, acc)`` with ``m`` the largest score, ``l = sum_j exp(s_j - m)``
+    and ``acc = sum_j exp(s_j - m) V_j``.  An empty subset gives
+    ``(-inf, 0, 0)``."""
+    if K.shape[0] == 0:
+        return -math.inf, 0.0, np.zeros(V.shape[1], np.float64)
+    s = scale * (K @ qv)
+    m = float(np.max(s))
+    w = np.exp(s - m)
+    return m, float(np.sum(w)), w @ V
+
+
+def merge_states(states) -> np.ndarray:
+    """Softmax over the union of disjoint key subsets from their states:
+    with ``M = max m_i``, ``out = sum_i e^(m_i - M) acc_i / sum_i e^(m_i - M) l_i``.
+    This is the exact regrouping of the sums in the softmax definition
+    ("Inside SGLang", Step 3: Look inside the forward pass), the same algebra
+    a split-KV decode uses to join its chunks."""
+    M = max(m for m, _, _ in states)
+    num = sum(math.exp(m - M) * acc for m, _, acc in states if m != -math.inf)
+    den = sum(math.exp(m - M) * l for m, l, _ in states if m != -math.inf)
+    return num / den
+
+
+def cascade_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_lens,
+                             group_start, group_len, group_depth, member_off, members,
+                             num_kv_heads: int, sm_scale=None, requests=None) -> np.ndarray:
+    """DECODE attention computed group by group, float64.
+
+    A group is a run of positions ``[group_start[j], group_start[j] +
+    group_len[j])`` shared by the requests ``members[member_off[j] :
+    member_off[j+1]]``; its keys are read once, from the row of its first
+    member, and every member's queries attend to them.  Request ``r``'s groups,
+    taken by ``group_depth``, cover positions ``[0, shared_len_r)`` back to back;
+    its own keys ``[shared_len_r, seq_lens[r])`` are the private tail.  The
+    output merges the states of the groups and the tail (``merge_states``).
+    Requests that share a prefix hold identical slot numbers there ("Inside
+    SGLang", Step 3: Paged KV and the kernels that read it), so when every
+    member's row agrees with its group's first member over the group's range,
+    this equals ``decode_attention``.  Returns [B, Hq, D] (or the listed
+    requests)."""
+    q = np.asarray(q)
+    B, Hq, D = q.shape
+    scale = default_scale(D) if sm_scale is None else float(sm_scale)
+    group_start = np.asarray(group_start, np.int64)
+    group_len = np.asarray(group_len, np.int64)
+    group_depth = np.asarray(group_depth, np.int64)
+    member_off = np.asarray(member_off, np.int64)
+    members = np.asarray(members, np.int64)
+    # each request's groups, in depth order
+    mine = [[] for _ in range(B)]
+    for j in range(group_start.size):
+        for r in members[member_off[j]: member_off[j + 1]]:
+            mine[int(r)].append((int(group_depth[j]), j))
+    want = np.arange(B) if requests is None else np.asarray(requests, dtype=np.int64)
+    out = np.zeros((want.size, Hq, D), np.float64)
+    for n, r in enumerate(want):
+        r = int(r)
+        qr = bf16_bits_to_f64(q[r])
+        pieces = []      # (K, V) of each group, then of the tail
+        shared = 0
+        for _, j in sorted(mine[r]):
+            first = int(members[member_off[j]])
+            a, e = int(group_start[j]), int(group_start[j] + group_len[j])
+            slots = np.asarray(req_to_token[int(req_pool_idx[first]), a:e], np.int64)
+            pieces.append((bf16_bits_to_f64(pool_k[slots]), bf16_bits_to_f64(pool_v[slots])))
+            shared = e
+        slots = np.asarray(req_to_token[int(req_pool_idx[r]), shared:int(seq_lens[r])], np.int64)
+        pieces.append((bf16_bits_to_f64(pool_k[slots]), bf16_bits_to_f64(pool_v[slots])))
+        for h in range(Hq):
+            kh = _kv_head_of(h, Hq, num_kv_heads)
+            out[n, h] = merge_states([partial_state(qr[h], K[:, kh], V[:, kh], scale)
+                                      for K, V in pieces])
+    return out

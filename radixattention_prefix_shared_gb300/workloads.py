@@ -204,6 +204,90 @@ class Workload:
         return pk, pv
 
 
+@dataclass
+class CascadeGroups:
+    """Runs of positions shared by several requests of one decode batch.
+
+    Group ``j`` covers positions ``[group_start[j], group_start[j] +
+    group_len[j])`` of every member's row; its members are
+    ``members[member_off[j]:member_off[j+1]]`` (indices into the decode batch)
+    and ``group_depth[j]`` is its rank among each member's groups, which cover
+    ``[0, shared_len)`` back to back.  In a radix tree these are the nodes with
+    two or more running requests below them.
+    """
+    group_start: np.ndarray    # int32 [G]
+    group_len: np.ndarray      # int32 [G]
+    group_depth: np.ndarray    # int32 [G]
+    member_off: np.ndarray     # int32 [G+1]
+    members: np.ndarray        # int32 [nnz]
+
+    @property
+    def n_groups(self) -> int:
+        return int(self.group_start.size)
+
+    @property
+    def max_members(self) -> int:
+        return int(np.diff(self.member_off).max()) if self.n_groups else 0
+
+    @property
+    def max_depth(self) -> int:
+        """Number of depth levels (largest depth + 1; 0 without groups)."""
+        return int(self.group_depth.max()) + 1 if self.n_groups else 0
+
+    def shared_lens(self, batch: int) -> np.ndarray:
+        """Per request: the end of its deepest group (0 if it is in none)."""
+        out = np.zeros(batch, np.int64)
+        for j in range(self.n_groups):
+            m = self.members[self.member_off[j]: self.member_off[j + 1]]
+            out[m] = np.maximum(out[m], int(self.group_start[j]) + int(self.group_len[j]))
+        return out
+
+
+def shared_prefix_groups(req_to_token: np.ndarray, req_pool_idx, seq_lens,
+                         min_members: int = 2) -> CascadeGroups:
+    """The shared-prefix groups of a decode batch, read off its rows.
+
+    Requests whose rows hold the same slot at a position share that token
+    ("Inside SGLang", Step 3: Paged KV and the kernels that read it -- shared
+    prefixes are identical leading slot numbers).  Starting at position 0, the
+    requests are split by their slot; a set of at least ``min_members``
+    requests forms a group that runs while all of them agree (and none has
+    ended), then the set splits again at the first disagreement: a compressed
+    trie over the slot sequences, i.e. the radix tree's nodes restricted to the
+    running requests.  Groups are listed by (depth, start, first member).
+    """
+    rtt = np.asarray(req_to_token)
+    rows = np.asarray(req_pool_idx, np.int64)
+    lens = np.asarray(seq_lens, np.int64)
+    found = []
+    work = [(np.nonzero(lens > 0)[0], 0, 0)]
+    while work:
+        mem, pos, depth = work.pop()
+        if mem.size < min_members:
+            continue
+        at = rtt[rows[mem], pos]
+        for v in np.unique(at):
+            sub = mem[at == v]
+            if sub.size < min_members:
+                continue
+            lim = int(lens[sub].min())
+            block = rtt[rows[sub], pos:lim]
+            agree = np.all(block == block[0], axis=0)
+            stop = np.nonzero(~agree)[0]
+            end = pos + (int(stop[0]) if stop.size else lim - pos)
+            found.append((depth, pos, end - pos, np.sort(sub)))
+            rest = sub[lens[sub] > end]
+            work.append((rest, end, depth + 1))
+    found.sort(key=lambda f: (f[0], f[1], int(f[3][0])))
+    off = np.zeros(len(found) + 1, np.int32)
+    off[1:] = np.cumsum([f[3].size for f in found])
+    cat = np.concatenate([f[3] for f in found]) if found else np.zeros(0)
+    return CascadeGroups(group_start=np.asarray([f[1] for f in found], np.int32),
+                         group_len=np.asarray([f[2] for f in found], np.int32),
+                         group_depth=np.asarray([f[0] for f in found], np.int32),
+                         member_off=off, members=cat.astype(np.int32))
+
+
 class PoolView:
     """Read-only ``pool[slots]`` access that regenerates rows on demand."""
 
@@ -512,6 +596,53 @@ def tree_of_thought_decode(seed: int = 1004, depth: int = 4, fanout: int = 4,
     # tails past the last step still point at poisoned slots (filled above for
     # the step-0 lengths; positions ctx_len+1.. were overwritten step by step)
     return w
+
+
+def random_tree_decode(seed: int = 1006, dims: Dims | None = None, fanouts=(3, 3, 2),
+                       seg_len=(1, 300), own_len=(0, 40), n_solo: int = 2,
+                       pool_size: int = 1 << 16, std: float = 1.0) -> Workload:
+    """Decode over a random prefix tree with ragged node lengths.
+
+    Below an implicit root, level ``l`` nodes have ``fanouts[l]`` children;
+    every node holds U[seg_len] tokens, each leaf is one decode request whose
+    row is its ancestors' tokens, then its own U[own_len] private tokens, then
+    the new one.  ``n_solo`` more requests share nothing.  The batch order is
+    shuffled, so no group's members are contiguous.  Slots come from one
+    seeded permutation of the pool.
+    """
+    dims = dims or Dims(16, 4, 128, pool_size, 1.0 / math.sqrt(128))
+    assert dims.pool_size == pool_size
+    g = _rng(seed, _S_LAYOUT + 100)
+    perm = g.permutation(pool_size).astype(np.int32)
+    pos = 0
+
+    def take(n):
+        nonlocal pos
+        out = perm[pos: pos + n]
+        pos += n
+        assert out.size == n, "pool too small"
+        return out
+
+    level = [np.zeros(0, np.int32)]
+    for f in fanouts:
+        level = [np.concatenate([ctx, take(int(g.integers(seg_len[0], seg_len[1] + 1)))])
+                 for ctx in level for _ in range(f)]
+    ctx = [np.concatenate([c, take(int(g.integers(own_len[0], own_len[1] + 1)))]) for c in level]
+    ctx += [take(int(g.integers(seg_len[0], 2 * seg_len[1] + 1))) for _ in range(n_solo)]
+    ctx = [ctx[i] for i in g.permutation(len(ctx))]
+    live = np.concatenate(ctx)
+    _, first = np.unique(live, return_index=True)
+    live = live[np.sort(first)]
+    return build_workload("random_tree_decode", dims, seed, decode_ctx=ctx, std=std,
+                          live_slots=live, slot_source=perm[pos:],
+                          recipe=dict(fanouts=list(fanouts), seg_len=list(seg_len),
+                                      own_len=list(own_len), n_solo=n_solo, pool=pool_size))
+
+
+def tree_groups(w: Workload, step: int = 0) -> CascadeGroups:
+    """Shared-prefix groups of decode step ``step`` of a tree workload."""
+    b = w.decode[step]
+    return shared_prefix_groups(w.req_to_token, b.req_pool_idx, b.seq_lens)
 
 
 def _eviction_layout(g: np.random.Generator, pool_size: int, live_lens: np.ndarray,
