@@ -163,7 +163,7 @@ def barrier():
 class Step:
     """Device buffers of one workload and the launches of one step."""
 
-    def __init__(self, w: W.Workload, device):
+    def __init__(self, w: W.Workload, device, cascade: str = "off"):
         import torch
         from radixattention_prefix_shared_gb300 import binding as B
         self.B, self.torch, self.w, self.dev = B, torch, w, device
@@ -193,11 +193,28 @@ class Step:
             t["decode"][0]["v_new"] = self.v_all[n_ext:]
         self.ws_ext = B.new_workspace(256, device)
         self.out_ext = torch.empty_like(t["extend"]["q"]) if w.extend is not None else None
+        # cascade decode: the shared-prefix groups of every decode step, read
+        # off its rows once here (the host side of a serving loop keeps them
+        # in its radix tree); "auto" uses them when the batch shares prefixes
+        self.groups = []
+        if cascade != "off" and w.decode:
+            self.groups = [W.tree_groups(w, s) for s in range(len(w.decode))]
+            if cascade == "auto" and not any(g.n_groups for g in self.groups):
+                self.groups = []
+        self.cascade = bool(self.groups)
+        self.groups_dev = [[W.int_tensor(a, device) for a in (g.group_start, g.group_len, g.group_depth,
+                                                              g.member_off, g.members)]
+                           for g in self.groups]
         self.out_dec, self.ws_dec = [], []
-        for b, tb in zip(w.decode, t["decode"]):
+        for s, (b, tb) in enumerate(zip(w.decode, t["decode"])):
             self.out_dec.append(torch.empty_like(tb["q"]))
             dims = B.make_dims(self.Hq, self.Hkv, self.D, d.pool_size)
-            self.ws_dec.append(B.new_workspace(B.decode_workspace_bytes(b.q.shape[0], int(b.seq_lens.max()), dims), device))
+            if self.cascade:
+                nb = B.cascade_decode_workspace_bytes(b.q.shape[0], int(b.seq_lens.max()),
+                                                      max(self.groups[s].max_depth, 1), dims)
+            else:
+                nb = B.decode_workspace_bytes(b.q.shape[0], int(b.seq_lens.max()), dims)
+            self.ws_dec.append(B.new_workspace(nb, device))
         self.tokens = (w.extend.total_extend if w.extend is not None else 0) + sum(b.q.shape[0] for b in w.decode)
         self.launches = 0
 
@@ -224,10 +241,19 @@ class Step:
             if s > 0:
                 B.sgl_store_kv(tb["k_new"], tb["v_new"], tb["slots"], t["pool_k"], t["pool_v"])
                 launches += 1
-            B.sgl_decode_attention(tb["q"], t["pool_k"], t["pool_v"], t["req_to_token"], tb["req_pool_idx"],
-                                   tb["seq_lens"], self.out_dec[s], max_seq_len=int(b.seq_lens.max()),
-                                   workspace=self.ws_dec[s])
-            launches += 3
+            if self.cascade:
+                g = self.groups[s]
+                B.sgl_cascade_decode_attention(tb["q"], t["pool_k"], t["pool_v"], t["req_to_token"],
+                                               tb["req_pool_idx"], tb["seq_lens"], *self.groups_dev[s],
+                                               self.out_dec[s], max_seq_len=int(b.seq_lens.max()),
+                                               max_group_members=max(g.max_members, 1),
+                                               max_depth=max(g.max_depth, 1), workspace=self.ws_dec[s])
+                launches += 4 if g.n_groups else 3   # plan, groups, split, combine
+            else:
+                B.sgl_decode_attention(tb["q"], t["pool_k"], t["pool_v"], t["req_to_token"],
+                                       tb["req_pool_idx"], tb["seq_lens"], self.out_dec[s],
+                                       max_seq_len=int(b.seq_lens.max()), workspace=self.ws_dec[s])
+                launches += 3                        # plan, split, combine
         if ev is not None:
             ev[3].record()
         self.launches = launches
@@ -254,7 +280,8 @@ class Step:
         o.ws_ext = self.B.new_workspace(256, self.dev)
         o.out_ext = torch.empty_like(self.out_ext) if self.out_ext is not None else None
         o.out_dec = [torch.empty_like(x) for x in self.out_dec]
-        o.ws_dec = [torch.empty_like(x) for x in self.ws_dec]
+        o.ws_dec = [torch.zeros_like(x) for x in self.ws_dec]
+        o.groups_dev = [[x.clone() for x in g] for g in self.groups_dev]
         return o
 
     # inputs that arrive from the host every step, and the results read back
@@ -267,6 +294,8 @@ class Step:
             outs.append(self.out_ext)
         for s, tb in enumerate(self.t["decode"]):
             ins += [tb["q"], tb["req_pool_idx"], tb["seq_lens"]]
+            if self.cascade:
+                ins += self.groups_dev[s]
             if s > 0:
                 ins += [tb["k_new"], tb["v_new"], tb["slots"]]
             outs.append(self.out_dec[s])
@@ -285,7 +314,7 @@ def small_kwargs(args):
     return SMALL.get(args.config, {}) if getattr(args, "small", False) else {}
 
 
-def work_of(w: W.Workload):
+def work_of(w: W.Workload, groups=()):
     d = w.dims
     flops = 0
     ext_bytes = 0
@@ -294,9 +323,14 @@ def work_of(w: W.Workload):
         flops = WM.extend_flops(e.prefix_lens, e.extend_lens, d.num_q_heads, d.head_dim)
         ext_bytes = WM.extend_bytes(e.prefix_lens, e.extend_lens, d.num_q_heads, d.num_kv_heads, d.head_dim)
     dec_bytes = sum(WM.decode_bytes(b.seq_lens, d.num_q_heads, d.num_kv_heads, d.head_dim) for b in w.decode)
+    # with cascade groups each shared group's keys are read once per step
+    dec_unique = sum(WM.cascade_decode_bytes(g.group_len, g.shared_lens(b.q.shape[0]), b.seq_lens,
+                                             d.num_q_heads, d.num_kv_heads, d.head_dim)
+                     for g, b in zip(groups, w.decode)) if groups else dec_bytes
     n_new = (w.extend.total_extend if w.extend is not None else 0) + sum(b.q.shape[0] for b in w.decode)
     st_bytes = WM.store_kv_bytes(n_new, d.num_kv_heads, d.head_dim)
-    return dict(extend_flops=flops, extend_bytes=ext_bytes, decode_bytes=dec_bytes, store_bytes=st_bytes)
+    return dict(extend_flops=flops, extend_bytes=ext_bytes, decode_bytes=dec_bytes,
+                decode_read_once_bytes=dec_unique, store_bytes=st_bytes)
 
 
 def gpu_arm(args):
@@ -308,8 +342,8 @@ def gpu_arm(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.make(args.config, seed=1000 + args.config + 7919 * rank, **small_kwargs(args))
-    step = Step(w, dev)
-    work = work_of(w)
+    step = Step(w, dev, args.cascade)
+    work = work_of(w, step.groups)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
     stream = torch.cuda.current_stream()
 
@@ -398,18 +432,25 @@ def gpu_arm(args):
                              "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
                              "algorithmic_tflop": round(work["extend_flops"] / 1e12, 4)}
     if work["decode_bytes"]:
-        gbs = work["decode_bytes"] / (ms_dec / 1e3) / 1e9
+        # the roofline counts the bytes the path must read: every key once per
+        # request (plain decode), or once per shared group (cascade)
+        alg = work["decode_read_once_bytes"] if step.cascade else work["decode_bytes"]
+        gbs = alg / (ms_dec / 1e3) / 1e9
         kernels["decode"] = {"ms": round(ms_dec, 4), "gbs": round(gbs, 1),
                              "frac_of_hbm_peak": round(gbs / pk["hbm_gbs"], 4),
-                             "algorithmic_gb": round(work["decode_bytes"] / 1e9, 4),
-                             "launches_per_step": 3 * len(w.decode)}
+                             "algorithmic_gb": round(alg / 1e9, 4),
+                             "path": "cascade" if step.cascade else "plain"}
+        if step.cascade:
+            kernels["decode"]["logical_gb"] = round(work["decode_bytes"] / 1e9, 4)
+            kernels["decode"]["logical_gbs"] = round(work["decode_bytes"] / (ms_dec / 1e3) / 1e9, 1)
     gbs_st = work["store_bytes"] / (ms_store / 1e3) / 1e9
     kernels["store_kv"] = {"ms": round(ms_store, 4), "gbs": round(gbs_st, 1),
                            "algorithmic_gb": round(work["store_bytes"] / 1e9, 4)}
     wl = WORKLOAD_NAMES[args.config]
     if "decode" in kernels and (ms_dec >= ms_ext or "extend" not in kernels):
         ach = kernels["decode"]["gbs"]
-        roof = {"kernel": "decode (plan + split + combine)", "bound": "hbm", "achieved": ach,
+        roof = {"kernel": "cascade decode (plan + groups + split + combine)" if step.cascade
+                else "decode (plan + split + combine)", "bound": "hbm", "achieved": ach,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                 "traffic": measured_traffic("decode", wl), "peak_source": pk["source"]}
     else:
@@ -428,6 +469,7 @@ def gpu_arm(args):
                    "extend_tokens": int(w.extend.total_extend) if w.extend is not None else 0,
                    "decode_requests": int(sum(b.q.shape[0] for b in w.decode)),
                    "query_tokens_per_step": int(step.tokens), "parallelism": f"replicas{world}",
+                   "decode_path": ("cascade" if step.cascade else "plain") if w.decode else None,
                    "l2": "flushed between steps (256 MiB write)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_bytes),
                 "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e_ms, 4),
@@ -549,6 +591,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOAD_NAMES))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cascade", choices=["auto", "on", "off"], default="auto",
+                    help="decode through shared-prefix groups (auto: when the batch shares prefixes)")
     ap.add_argument("--small", action="store_true",
                     help="reduced pool / batch of the workload, for profiler captures")
     args = ap.parse_args(argv)

@@ -180,9 +180,60 @@ sgl_status sgl_decode_attention_noalloc(const void* q, const void* pool_k, const
                                         int32_t max_seq_len, void* out, const sgl_attn_dims* dims,
                                         sgl_stream_t stream);
 
+/*
+ * sgl_cascade_decode_attention -- decode attention that reads each shared
+ * prefix once per group of requests.
+ *
+ * Computes what sgl_decode_attention computes (same arguments, same output),
+ * given a description of the keys that several requests of the batch share.
+ * Requests that share a prefix hold identical slot numbers in the leading
+ * entries of their rows ("Inside SGLang", Step 3: Paged KV and the kernels
+ * that read it), so the softmax over a request's keys splits into one state
+ * per shared group plus one for its private tail, merged exactly (the
+ * regrouping of the softmax sums that also joins the split-KV chunks).  A
+ * group's keys are gathered once and all of its members' query heads attend
+ * to them on the tensor cores; the tails run as plain split-KV decode.
+ *   group_start, group_len : int32 [n_groups]  group j covers positions
+ *                            [group_start[j], group_start[j] + group_len[j])
+ *                            of every member's row; group_len >= 1
+ *   group_depth            : int32 [n_groups]  j's rank among each member's
+ *                            groups, in [0, max_depth)
+ *   group_member_off       : int32 [n_groups + 1]  CSR offsets (first 0)
+ *   group_members          : int32 [group_member_off[n_groups]]  member
+ *                            requests (indices into the batch)
+ *   n_groups               : host value (<= 65535); 0 = plain decode
+ *   max_group_members      : >= the largest member count (host; sizes the grid)
+ *   max_depth              : >= the largest group_depth + 1 (host; sizes the
+ *                            workspace)
+ *   workspace              : >= sgl_cascade_decode_workspace_bytes(batch,
+ *                            max_seq_len, max_depth, dims); the first 256
+ *                            bytes must be zero-filled once before first use:
+ *                            word 0 is set to a nonzero code if a bounded
+ *                            on-chip wait of the group pass gave up (the
+ *                            output is then incomplete); it is never cleared.
+ * Preconditions (sgl_check_cascade_groups verifies them): every member's row
+ * holds the same slots as the group's first member over the group's range
+ * (the keys are read from the first member's row); each request's groups,
+ * ordered by depth 0, 1, ..., cover [0, shared_len) back to back with
+ * shared_len <= seq_len; a request's keys [shared_len, seq_len) are its
+ * private tail (possibly empty).  A request in no group is plain decode.
+ * Member indices outside [0, batch) and depths outside [0, max_depth) are
+ * skipped; other violations give undefined results but no out-of-bounds
+ * write.
+ */
+sgl_status sgl_cascade_decode_attention(
+    const void* q, const void* pool_k, const void* pool_v, const int32_t* req_to_token,
+    int32_t rtt_rows, int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+    int32_t batch, int32_t max_seq_len, const int32_t* group_start, const int32_t* group_len,
+    const int32_t* group_depth, const int32_t* group_member_off, const int32_t* group_members,
+    int32_t n_groups, int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
+    size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream);
+
 /* Workspace sizes (host only; no device call). */
 size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims);
 size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_attn_dims* dims);
+size_t sgl_cascade_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t max_depth,
+                                          const sgl_attn_dims* dims);
 
 /*
  * Checked mode.  Each call validates the index values in device memory with a
@@ -196,8 +247,22 @@ size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_
  *   kind 4: prefix+extend or seq_len > rtt_stride  a = request, c = length
  *   kind 5: sum(extend_lens) != total_extend or a length above the host max
  *   kind 6: duplicate slot in one store_kv call  a = second index, c = slot
+ *   kind 7: malformed cascade group (offsets, member count above the host
+ *           max, member outside the batch, depth outside [0, max_depth),
+ *           length < 1)                      a = group, b = which check, c = value
+ *   kind 8: group range past a member's seq_len or past rtt_stride
+ *                                            a = group, b = member (-1: stride), c = end
+ *   kind 9: a member's slot differs from the first member's (not shared)
+ *                                            a = group, b = position, c = member
+ *   kind 10: a request's groups do not cover [0, shared_len) back to back
+ *           (two groups at one depth, a gap, or a wrong start)
+ *                                            a = request, b = depth, c = group / start
  * sgl_check_store_kv_indices needs a scratch bitmap of (pool_size+7)/8 bytes
  * (rounded up to 16) in `bitmap`; it is cleared by the call.
+ * sgl_check_cascade_groups needs sgl_check_cascade_scratch_bytes(batch,
+ * max_depth) bytes of scratch (overwritten by the call); it checks the
+ * groups only -- pair it with sgl_check_decode_indices for rows, lengths and
+ * slot ranges.
  */
 sgl_status sgl_check_store_kv_indices(const int32_t* slots, int32_t n, int64_t pool_size,
                                       void* bitmap, size_t bitmap_bytes, int32_t* d_error,
@@ -211,6 +276,15 @@ sgl_status sgl_check_decode_indices(const int32_t* req_to_token, int32_t rtt_row
                                     const int32_t* req_pool_idx, const int32_t* seq_lens,
                                     int32_t batch, int32_t max_seq_len, int64_t pool_size,
                                     int32_t* d_error, sgl_stream_t stream);
+size_t sgl_check_cascade_scratch_bytes(int32_t batch, int32_t max_depth);
+sgl_status sgl_check_cascade_groups(const int32_t* req_to_token, int32_t rtt_rows,
+                                    int32_t rtt_stride, const int32_t* req_pool_idx,
+                                    const int32_t* seq_lens, int32_t batch,
+                                    const int32_t* group_start, const int32_t* group_len,
+                                    const int32_t* group_depth, const int32_t* group_member_off,
+                                    const int32_t* group_members, int32_t n_groups,
+                                    int32_t max_group_members, int32_t max_depth, void* scratch,
+                                    size_t scratch_bytes, int32_t* d_error, sgl_stream_t stream);
 
 #ifdef __cplusplus
 }

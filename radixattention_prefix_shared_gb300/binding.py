@@ -50,6 +50,15 @@ _SIGS = {
                                                 c_i32, c_i64, c_vp, c_vp]),
     "sgl_check_decode_indices": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i64,
                                                 c_vp, c_vp]),
+    "sgl_cascade_decode_attention": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp,
+                                                    c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
+                                                    c_i32, c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims),
+                                                    c_vp]),
+    "sgl_cascade_decode_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, _P(sgl_attn_dims)]),
+    "sgl_check_cascade_scratch_bytes": (c_size, [c_i32, c_i32]),
+    "sgl_check_cascade_groups": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                                c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_size, c_vp,
+                                                c_vp]),
 }
 
 _lib = None
@@ -188,3 +197,51 @@ def sgl_check_decode_indices(req_to_token, req_pool_idx, seq_lens, *, max_seq_le
         _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx),
         _ptr(seq_lens), int(req_pool_idx.shape[0]), int(max_seq_len), int(pool_size), _ptr(d_error),
         _stream(stream)))
+
+
+# ----------------------------------------------------------------- cascade
+
+def cascade_decode_workspace_bytes(batch, max_seq_len, max_depth, dims: sgl_attn_dims) -> int:
+    return int(lib().sgl_cascade_decode_workspace_bytes(int(batch), int(max_seq_len), int(max_depth),
+                                                        ctypes.byref(dims)))
+
+
+def sgl_cascade_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_lens,
+                                 group_start, group_len, group_depth, group_member_off, group_members,
+                                 out=None, *, max_seq_len, max_group_members, max_depth,
+                                 workspace=None, sm_scale=0.0, stream=None):
+    """Decode attention with shared-prefix groups read once per group.
+
+    ``group_*`` are int32 device tensors (CSR members); ``max_seq_len``,
+    ``max_group_members`` and ``max_depth`` are host values.  A new workspace
+    is zero-filled; a reused one must keep its first 256 bytes zero."""
+    import torch
+    d = _dims_for(q, pool_k, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    B = int(q.shape[0])
+    G = int(group_start.shape[0])
+    if workspace is None:
+        workspace = new_workspace(cascade_decode_workspace_bytes(B, max_seq_len, max_depth, d), q.device)
+    _check("sgl_cascade_decode_attention", lib().sgl_cascade_decode_attention(
+        _ptr(q), _ptr(pool_k), _ptr(pool_v), _ptr(req_to_token), int(req_to_token.shape[0]),
+        int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(seq_lens), B, int(max_seq_len),
+        _ptr(group_start), _ptr(group_len), _ptr(group_depth), _ptr(group_member_off), _ptr(group_members),
+        G, int(max_group_members), int(max_depth), _ptr(out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), ctypes.byref(d), _stream(stream)))
+    return out
+
+
+def sgl_check_cascade_groups(req_to_token, req_pool_idx, seq_lens, group_start, group_len, group_depth,
+                             group_member_off, group_members, *, max_group_members, max_depth, d_error,
+                             scratch=None, stream=None):
+    import torch
+    B = int(req_pool_idx.shape[0])
+    need = int(lib().sgl_check_cascade_scratch_bytes(B, int(max_depth)))
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=req_to_token.device)
+    _check("sgl_check_cascade_groups", lib().sgl_check_cascade_groups(
+        _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx),
+        _ptr(seq_lens), B, _ptr(group_start), _ptr(group_len), _ptr(group_depth), _ptr(group_member_off),
+        _ptr(group_members), int(group_start.shape[0]), int(max_group_members), int(max_depth),
+        _ptr(scratch), int(scratch.numel()), _ptr(d_error), _stream(stream)))

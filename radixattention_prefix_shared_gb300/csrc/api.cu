@@ -124,6 +124,85 @@ __global__ void check_sum_kernel(const int32_t* __restrict__ lens, int32_t batch
   }
 }
 
+// Cascade groups, one block per group (grid-stride): structure, member
+// ranges, shared slots, and each (request, depth) claimed by one group only.
+__global__ void check_groups_kernel(const int32_t* __restrict__ rtt, int32_t rtt_rows,
+                                    int32_t stride, const int32_t* __restrict__ rpi,
+                                    const int32_t* __restrict__ seq_lens, int32_t batch,
+                                    const int32_t* __restrict__ gstart,
+                                    const int32_t* __restrict__ glen,
+                                    const int32_t* __restrict__ gdepth,
+                                    const int32_t* __restrict__ moff,
+                                    const int32_t* __restrict__ mem, int32_t n_groups,
+                                    int32_t max_members, int32_t max_depth,
+                                    int32_t* __restrict__ owner, int32_t* err) {
+  __shared__ int bad;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && moff[0] != 0) report(err, 7, 0, 0, moff[0]);
+  for (int32_t j = blockIdx.x; j < n_groups; j += gridDim.x) {
+    const int32_t a = moff[j], b = moff[j + 1];
+    const int32_t st = gstart[j], ln = glen[j], dp = gdepth[j];
+    if (threadIdx.x == 0) {
+      bad = 0;
+      if (b < a || b - a > max_members) bad = 1, report(err, 7, j, 0, b - a);
+      else if (dp < 0 || dp >= max_depth) bad = 1, report(err, 7, j, 1, dp);
+      else if (ln < 1 || st < 0) bad = 1, report(err, 7, j, 2, ln < 1 ? ln : st);
+      else if ((int64_t)st + ln > stride) bad = 1, report(err, 8, j, -1, st + ln);
+    }
+    __syncthreads();
+    if (!bad) {
+      for (int32_t k = a + threadIdx.x; k < b; k += blockDim.x) {
+        const int32_t r = mem[k];
+        if (r < 0 || r >= batch) {
+          report(err, 7, j, 3, r);
+          atomicOr(&bad, 1);
+          continue;
+        }
+        const int32_t row = rpi[r];
+        if (row < 0 || row >= rtt_rows) {
+          report(err, 2, r, 0, row);
+          atomicOr(&bad, 1);
+          continue;
+        }
+        if (st + ln > seq_lens[r]) report(err, 8, j, r, st + ln);
+        if (atomicCAS(&owner[(int64_t)r * max_depth + dp], -1, j) != -1) report(err, 10, r, dp, j);
+      }
+    }
+    __syncthreads();
+    if (!bad && b > a) {
+      const int32_t* ref = rtt + (int64_t)rpi[mem[a]] * stride + st;
+      const int64_t n = (int64_t)(b - a - 1) * ln;
+      for (int64_t t = threadIdx.x; t < n; t += blockDim.x) {
+        const int32_t r = mem[a + 1 + (int32_t)(t / ln)];
+        const int32_t i = (int32_t)(t % ln);
+        if (rtt[(int64_t)rpi[r] * stride + st + i] != ref[i]) report(err, 9, j, st + i, r);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Each request's groups, by depth, must cover [0, shared_len) back to back.
+__global__ void check_tiling_kernel(const int32_t* __restrict__ owner, int32_t batch,
+                                    int32_t max_depth, const int32_t* __restrict__ gstart,
+                                    const int32_t* __restrict__ glen, int32_t* err) {
+  const int32_t r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= batch) return;
+  int32_t pos = 0;
+  bool ended = false;
+  for (int32_t d = 0; d < max_depth; ++d) {
+    const int32_t j = owner[(int64_t)r * max_depth + d];
+    if (j < 0) {
+      ended = true;
+      continue;
+    }
+    if (ended || gstart[j] != pos) {
+      report(err, 10, r, d, gstart[j]);
+      return;
+    }
+    pos += glen[j];
+  }
+}
+
 sgl_status last_launch() { return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA; }
 
 }  // namespace
@@ -175,6 +254,14 @@ size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_
   if (dims == nullptr || dims->num_kv_heads <= 0 || dims->num_q_heads <= 0) return 0;
   return decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads, dims->num_kv_heads,
                                 dims->head_dim);
+}
+
+size_t sgl_cascade_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t max_depth,
+                                          const sgl_attn_dims* dims) {
+  if (dims == nullptr || dims->num_kv_heads <= 0 || dims->num_q_heads <= 0 || max_depth < 0)
+    return 0;
+  return decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads, dims->num_kv_heads,
+                                dims->head_dim, true, max_depth);
 }
 
 sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_new,
@@ -261,6 +348,99 @@ sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* p
   a.head_dim = dims->head_dim;
   a.sm_scale = scale;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgl_status sgl_cascade_decode_attention(
+    const void* q, const void* pool_k, const void* pool_v, const int32_t* req_to_token,
+    int32_t rtt_rows, int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+    int32_t batch, int32_t max_seq_len, const int32_t* group_start, const int32_t* group_len,
+    const int32_t* group_depth, const int32_t* group_member_off, const int32_t* group_members,
+    int32_t n_groups, int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
+    size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+  float scale;
+  sgl_status st = check_dims(dims, &scale);
+  if (st != SGL_OK) return st;
+  if (batch < 0 || max_seq_len < 0 || n_groups < 0 || max_group_members < 0 || max_depth < 0)
+    return SGL_ERR_INVALID_ARG;
+  if (batch == 0) return SGL_OK;
+  if (max_seq_len < 1) return SGL_ERR_INVALID_ARG;
+  if (!q || !pool_k || !pool_v || !req_to_token || !req_pool_idx || !seq_lens || !out)
+    return SGL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool_k) || !aligned16(pool_v)) return SGL_ERR_INVALID_ARG;
+  if (rtt_rows <= 0 || rtt_stride <= 0) return SGL_ERR_INVALID_ARG;
+  if (n_groups > 0) {
+    if (!group_start || !group_len || !group_depth || !group_member_off || !group_members)
+      return SGL_ERR_INVALID_ARG;
+    if (max_depth < 1 || max_group_members < 1) return SGL_ERR_INVALID_ARG;
+    if (n_groups > 65535) return SGL_ERR_UNSUPPORTED;
+  }
+  const size_t need = decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads,
+                                             dims->num_kv_heads, dims->head_dim, true, max_depth);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return SGL_ERR_WORKSPACE;
+  DecodeArgs a;
+  a.q = q;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.req_to_token = req_to_token;
+  a.rtt_stride = rtt_stride;
+  a.req_pool_idx = req_pool_idx;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.max_seq_len = max_seq_len;
+  a.out = out;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.head_dim = dims->head_dim;
+  a.sm_scale = scale;
+  a.cascade = true;
+  a.group_start = group_start;
+  a.group_len = group_len;
+  a.group_depth = group_depth;
+  a.group_member_off = group_member_off;
+  a.group_members = group_members;
+  a.n_groups = n_groups;
+  a.max_group_members = max_group_members;
+  a.max_depth = max_depth;
+  return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sgl_check_cascade_scratch_bytes(int32_t batch, int32_t max_depth) {
+  if (batch <= 0 || max_depth <= 0) return 16;
+  return ((size_t)batch * (size_t)max_depth * sizeof(int32_t) + 15) / 16 * 16;
+}
+
+sgl_status sgl_check_cascade_groups(const int32_t* req_to_token, int32_t rtt_rows,
+                                    int32_t rtt_stride, const int32_t* req_pool_idx,
+                                    const int32_t* seq_lens, int32_t batch,
+                                    const int32_t* group_start, const int32_t* group_len,
+                                    const int32_t* group_depth, const int32_t* group_member_off,
+                                    const int32_t* group_members, int32_t n_groups,
+                                    int32_t max_group_members, int32_t max_depth, void* scratch,
+                                    size_t scratch_bytes, int32_t* d_error, sgl_stream_t stream) {
+  if (batch < 0 || n_groups < 0 || max_group_members < 0 || max_depth < 0 || rtt_rows <= 0 ||
+      rtt_stride <= 0 || d_error == nullptr)
+    return SGL_ERR_INVALID_ARG;
+  if (batch == 0 || n_groups == 0) return SGL_OK;
+  if (!req_to_token || !req_pool_idx || !seq_lens || !group_start || !group_len || !group_depth ||
+      !group_member_off || !group_members || max_depth < 1)
+    return SGL_ERR_INVALID_ARG;
+  const size_t need = sgl_check_cascade_scratch_bytes(batch, max_depth);
+  if (scratch == nullptr || scratch_bytes < need) return SGL_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0xFF, need, s) != cudaSuccess) return SGL_ERR_CUDA;
+  int32_t* owner = static_cast<int32_t*>(scratch);
+  const unsigned blocks = (unsigned)(n_groups < 4096 ? n_groups : 4096);
+  check_groups_kernel<<<blocks, 256, 0, s>>>(req_to_token, rtt_rows, rtt_stride, req_pool_idx,
+                                             seq_lens, batch, group_start, group_len, group_depth,
+                                             group_member_off, group_members, n_groups,
+                                             max_group_members, max_depth, owner, d_error);
+  check_tiling_kernel<<<(unsigned)((batch + 255) / 256), 256, 0, s>>>(owner, batch, max_depth,
+                                                                      group_start, group_len,
+                                                                      d_error);
+  return last_launch();
 }
 
 sgl_status sgl_check_store_kv_indices(const int32_t* slots, int32_t n, int64_t pool_size,

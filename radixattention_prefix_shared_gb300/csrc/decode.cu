@@ -23,6 +23,11 @@
 //                 output directly; others write their partial state;
 //   3. combine -- one warp per (request, query head) merges the partial
 //                 states of multi-split requests (max-rescaled sums).
+// Cascade decode (shared prefixes read once per group) runs the same three
+// kernels with a group pass before the split: the plan kernel derives each
+// request's shared length and group count from the groups, the split kernel
+// covers only the private tail [shared_len, seq_len), and the combine merges
+// the group states (written by the tensor-core group kernel) with the tail's.
 // Scores are kept in the log2 domain (scale * log2(e) folded into q) and the
 // running max is only moved when a score exceeds it by more than 2^8, which
 // keeps every exponentiated weight <= 256 in fp32 and makes rescaling rare.
@@ -54,8 +59,19 @@ struct Ws {
   int2* items;          // [max_items]
   int32_t* n_items;     // [1]
   int32_t* next_item;   // [Hkv] work counters (zeroed by the plan kernel)
-  float2* part_ml;      // [max_items, Hkv, G]  (max in log2 units, sum)
-  float* part_acc;      // [max_items, Hkv, G, D]
+  int2* req_info;       // [B] (shared_len, number of groups); cascade only, else null
+  float2* part_ml;      // [max_items + B*max_depth, Hkv, G]  (max in log2 units, sum)
+  float* part_acc;      // [max_items + B*max_depth, Hkv, G, D]
+};
+
+// The groups of a cascade decode (all null / 0 for plain decode).
+struct Groups {
+  const int32_t* start;
+  const int32_t* len;
+  const int32_t* depth;
+  const int32_t* member_off;
+  const int32_t* members;
+  int32_t n_groups, max_depth;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -64,8 +80,10 @@ inline int64_t max_items_for(int32_t batch, int32_t max_seq_len) {
   return (int64_t)batch * ((max_seq_len + kChunk - 1) / kChunk);
 }
 
+// partial-state entries: the split items, then (cascade) B x max_depth group states
 inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G, int32_t D,
-                        void* base, Ws* ws) {
+                        int32_t max_depth, bool cascade, void* base, Ws* ws) {
+  const int64_t n_part = max_items + (cascade ? (int64_t)batch * max_depth : 0);
   size_t off = 0;
   size_t o_start = off;
   off = align256(off + sizeof(int32_t) * (size_t)(batch + 1));
@@ -75,16 +93,19 @@ inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G
   off = align256(off + sizeof(int32_t));
   size_t o_next = off;
   off = align256(off + sizeof(int32_t) * (size_t)Hkv);
+  size_t o_info = off;
+  if (cascade) off = align256(off + sizeof(int2) * (size_t)batch);
   size_t o_ml = off;
-  off = align256(off + sizeof(float2) * (size_t)max_items * Hkv * G);
+  off = align256(off + sizeof(float2) * (size_t)n_part * Hkv * G);
   size_t o_acc = off;
-  off = align256(off + sizeof(float) * (size_t)max_items * Hkv * G * D);
+  off = align256(off + sizeof(float) * (size_t)n_part * Hkv * G * D);
   if (ws && base) {
     char* b = static_cast<char*>(base);
     ws->item_start = reinterpret_cast<int32_t*>(b + o_start);
     ws->items = reinterpret_cast<int2*>(b + o_items);
     ws->n_items = reinterpret_cast<int32_t*>(b + o_n);
     ws->next_item = reinterpret_cast<int32_t*>(b + o_next);
+    ws->req_info = cascade ? reinterpret_cast<int2*>(b + o_info) : nullptr;
     ws->part_ml = reinterpret_cast<float2*>(b + o_ml);
     ws->part_acc = reinterpret_cast<float*>(b + o_acc);
   }
@@ -103,20 +124,45 @@ struct Params {
   int32_t batch, Hq, Hkv;
   float scale_log2;
   Ws ws;
+  int64_t group_base;  // first partial entry of the group states (= max_items)
+  int32_t max_depth;   // group states per request (cascade), else 0
 };
 
 // ---------------------------------------------------------------- plan
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ seq_lens,
                                                            int32_t batch, int64_t max_items,
-                                                           int32_t Hkv, Ws ws) {
+                                                           int32_t Hkv, Ws ws, Groups gr) {
   __shared__ int32_t warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int h = tid; h < Hkv; h += blockDim.x) ws.next_item[h] = 0;
+  if (ws.req_info != nullptr) {
+    // cascade: every membership raises its request's shared length to the
+    // group's end and its group count to the group's depth + 1
+    for (int r = tid; r < batch; r += blockDim.x) ws.req_info[r] = make_int2(0, 0);
+    __syncthreads();
+    for (int j = warp; j < gr.n_groups; j += blockDim.x >> 5) {
+      const int32_t a = gr.member_off[j], b = gr.member_off[j + 1];
+      const int32_t end = gr.start[j] + gr.len[j], cnt = gr.depth[j] + 1;
+      for (int32_t k = a + lane; k < b; k += 32) {
+        const int32_t r = gr.members[k];
+        if (r >= 0 && r < batch) {
+          atomicMax(&ws.req_info[r].x, end);
+          atomicMax(&ws.req_info[r].y, min(cnt, gr.max_depth));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // keys of request r handled by split items: the private tail [shared_len, seq_len)
+  auto tail_len = [&](int r) {
+    const int32_t sh = ws.req_info != nullptr ? __ldcg(&ws.req_info[r].x) : 0;
+    return max(seq_lens[r] - sh, 0);
+  };
   const int per = (batch + blockDim.x - 1) / blockDim.x;
   const int r0 = min(batch, tid * per), r1 = min(batch, r0 + per);
   int32_t local = 0;
-  for (int r = r0; r < r1; ++r) local += (max(seq_lens[r], 0) + kChunk - 1) / kChunk;
+  for (int r = r0; r < r1; ++r) local += (tail_len(r) + kChunk - 1) / kChunk;
   // block-wide exclusive scan of `local`
   int32_t inc = local;
 #pragma unroll
@@ -139,7 +185,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
   int32_t base = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0);
   for (int r = r0; r < r1; ++r) {
     ws.item_start[r] = base;
-    const int32_t ns = (max(seq_lens[r], 0) + kChunk - 1) / kChunk;
+    const int32_t ns = (tail_len(r) + kChunk - 1) / kChunk;
     for (int32_t s = 0; s < ns; ++s)
       if (base + s < max_items) ws.items[base + s] = make_int2(r, s);
     base += ns;
@@ -197,11 +243,13 @@ decode_split_kernel(Params p) {
     if (tid == 0) next = atomicAdd(&p.ws.next_item[kvh], 1);
     const int2 it = p.ws.items[item];
     const int r = it.x;
-    // the request's keys are cut into ceil(seq / kChunk) near-equal items
-    const int32_t seq = p.seq_lens[r];
-    const int32_t ns = (seq + kChunk - 1) / kChunk;
-    const int32_t base = seq / ns, rem = seq % ns;
-    const int32_t t0 = it.y * base + min(it.y, rem);
+    // the request's keys past its shared groups (all of them in plain decode)
+    // are cut into ceil(n / kChunk) near-equal items
+    const int2 info = p.ws.req_info != nullptr ? p.ws.req_info[r] : make_int2(0, 0);
+    const int32_t tail = max(p.seq_lens[r] - info.x, 0);
+    const int32_t ns = (tail + kChunk - 1) / kChunk;
+    const int32_t base = tail / ns, rem = tail % ns;
+    const int32_t t0 = info.x + it.y * base + min(it.y, rem);
     const int32_t n = base + (it.y < rem ? 1 : 0);
     const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride + t0;
     for (int i = tid; i < n; i += kThreads) s_slots[i] = rtt[i];
@@ -355,8 +403,7 @@ decode_split_kernel(Params p) {
       }
     }
     __syncthreads();
-    const int32_t s0 = p.ws.item_start[r];
-    const bool single = (p.ws.item_start[r + 1] - s0) == 1;
+    const bool single = ns == 1 && info.y == 0;
     for (int idx = tid; idx < G * D; idx += kThreads) {
       const int h = idx / D, d = idx % D;
       float M = -INFINITY;
@@ -393,11 +440,18 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(Params p) {
   if (gw >= (int64_t)p.batch * p.Hq) return;
   const int r = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
   const int32_t s0 = p.ws.item_start[r];
-  const int32_t ns = p.ws.item_start[r + 1] - s0;
-  if (ns <= 1 || s0 + ns > *p.ws.n_items) return;  // single split, or lengths above max_seq_len
+  const int32_t n_split = p.ws.item_start[r + 1] - s0;
+  const int32_t n_grp = p.ws.req_info != nullptr ? p.ws.req_info[r].y : 0;
+  if (n_grp == 0 && n_split <= 1) return;     // a single split wrote the output
+  if (s0 + n_split > *p.ws.n_items) return;   // lengths above max_seq_len
+  const int32_t ns = n_grp + n_split;
   const int G = p.Hq / p.Hkv;
   const int kvh = h / G, hh = h % G;
-  auto slot_of = [&](int32_t s) { return ((int64_t)(s0 + s) * p.Hkv + kvh) * G + hh; };
+  // states in key order: the groups by depth, then the tail's splits
+  auto slot_of = [&](int32_t s) {
+    const int64_t e = s < n_grp ? p.group_base + (int64_t)r * p.max_depth + s : (int64_t)(s0 + s - n_grp);
+    return (e * p.Hkv + kvh) * G + hh;
+  };
   float M = -INFINITY;
   for (int32_t s = lane; s < ns; s += 32) M = fmaxf(M, p.ws.part_ml[slot_of(s)].x);
 #pragma unroll
@@ -423,7 +477,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(Params p) {
 }
 
 template <int D, int G>
-sgl_status run(const Params& prm, int64_t max_items, cudaStream_t stream) {
+sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const GroupArgs* ga,
+               cudaStream_t stream) {
   constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
   constexpr size_t smem = (size_t)kStages * 2 * kTile * D * 2 + kChunk * sizeof(int32_t);
   static_assert(kWarps * G * (D + 2) * sizeof(float) <= (size_t)kStages * 2 * kTile * D * 2,
@@ -432,7 +487,12 @@ sgl_status run(const Params& prm, int64_t max_items, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return SGL_ERR_CUDA;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.Hkv, prm.ws);
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.Hkv, prm.ws,
+                                             gr);
+  if (ga != nullptr) {
+    const sgl_status st = launch_cascade_groups(*ga, stream);
+    if (st != SGL_OK) return st;
+  }
   int blocks_per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, kThreads, smem) !=
           cudaSuccess ||
@@ -449,12 +509,13 @@ sgl_status run(const Params& prm, int64_t max_items, cudaStream_t stream) {
 }
 
 template <int D>
-sgl_status run_g(int G, const Params& prm, int64_t max_items, cudaStream_t stream) {
+sgl_status run_g(int G, const Params& prm, int64_t max_items, const Groups& gr,
+                 const GroupArgs* ga, cudaStream_t stream) {
   switch (G) {
-    case 1: return run<D, 1>(prm, max_items, stream);
-    case 2: return run<D, 2>(prm, max_items, stream);
-    case 4: return run<D, 4>(prm, max_items, stream);
-    case 8: return run<D, 8>(prm, max_items, stream);
+    case 1: return run<D, 1>(prm, max_items, gr, ga, stream);
+    case 2: return run<D, 2>(prm, max_items, gr, ga, stream);
+    case 4: return run<D, 4>(prm, max_items, gr, ga, stream);
+    case 8: return run<D, 8>(prm, max_items, gr, ga, stream);
     default: return SGL_ERR_UNSUPPORTED;
   }
 }
@@ -462,9 +523,11 @@ sgl_status run_g(int G, const Params& prm, int64_t max_items, cudaStream_t strea
 }  // namespace
 
 size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, int32_t Hkv,
-                              int32_t D) {
-  if (batch <= 0 || max_seq_len <= 0 || Hkv <= 0) return 256;
-  return ws_layout(batch, max_items_for(batch, max_seq_len), Hkv, Hq / Hkv, D, nullptr, nullptr);
+                              int32_t D, bool cascade, int32_t max_depth) {
+  const size_t head = cascade ? kCascadeStatusBytes : 0;
+  if (batch <= 0 || max_seq_len <= 0 || Hkv <= 0) return head + 256;
+  return head + ws_layout(batch, max_items_for(batch, max_seq_len), Hkv, Hq / Hkv, D,
+                          cascade ? max_depth : 0, cascade, nullptr, nullptr);
 }
 
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -485,10 +548,50 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.Hq = a.num_q_heads;
   prm.Hkv = a.num_kv_heads;
   prm.scale_log2 = a.sm_scale * 1.4426950408889634f;
-  const size_t need = ws_layout(a.batch, max_items, a.num_kv_heads, G, a.head_dim, a.workspace, &prm.ws);
-  if (a.workspace == nullptr || a.workspace_bytes < need) return SGL_ERR_WORKSPACE;
-  if (a.head_dim == 128) return run_g<128>(G, prm, max_items, stream);
-  if (a.head_dim == 64) return run_g<64>(G, prm, max_items, stream);
+  // cascade: word 0 of the workspace is the group pass's status; the decode
+  // scratch follows the status bytes
+  const size_t head = a.cascade ? kCascadeStatusBytes : 0;
+  const int32_t max_depth = a.cascade ? a.max_depth : 0;
+  char* base = static_cast<char*>(a.workspace);
+  if (base == nullptr) return SGL_ERR_WORKSPACE;
+  const size_t need = head + ws_layout(a.batch, max_items, a.num_kv_heads, G, a.head_dim, max_depth,
+                                       a.cascade, base + head, &prm.ws);
+  if (a.workspace_bytes < need) return SGL_ERR_WORKSPACE;
+  prm.group_base = max_items;
+  prm.max_depth = max_depth;
+  Groups gr = {};
+  GroupArgs ga = {};
+  const bool groups = a.cascade && a.n_groups > 0;
+  if (groups) {
+    gr = Groups{a.group_start, a.group_len, a.group_depth, a.group_member_off, a.group_members,
+                a.n_groups, max_depth};
+    ga.q = a.q;
+    ga.pool_k = a.pool_k;
+    ga.pool_v = a.pool_v;
+    ga.req_to_token = a.req_to_token;
+    ga.rtt_stride = a.rtt_stride;
+    ga.req_pool_idx = a.req_pool_idx;
+    ga.group_start = a.group_start;
+    ga.group_len = a.group_len;
+    ga.group_depth = a.group_depth;
+    ga.member_off = a.group_member_off;
+    ga.members = a.group_members;
+    ga.batch = a.batch;
+    ga.n_groups = a.n_groups;
+    ga.max_members = a.max_group_members;
+    ga.max_depth = max_depth;
+    ga.part_ml = prm.ws.part_ml;
+    ga.part_acc = prm.ws.part_acc;
+    ga.part_base = max_items;
+    ga.status = reinterpret_cast<int*>(base);
+    ga.num_q_heads = a.num_q_heads;
+    ga.num_kv_heads = a.num_kv_heads;
+    ga.head_dim = a.head_dim;
+    ga.sm_scale = a.sm_scale;
+  }
+  const GroupArgs* gp = groups ? &ga : nullptr;
+  if (a.head_dim == 128) return run_g<128>(G, prm, max_items, gr, gp, stream);
+  if (a.head_dim == 64) return run_g<64>(G, prm, max_items, gr, gp, stream);
   return SGL_ERR_UNSUPPORTED;
 }
 

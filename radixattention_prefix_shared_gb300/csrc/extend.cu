@@ -115,6 +115,21 @@ struct Params {
   int32_t Hq, Hkv, g, tpt, rows_used;
   float scale_log2;
   int* status;
+  // group mode (cascade decode): group j covers positions
+  // [group_start[j], group_start[j] + group_len[j]) of its members' rows and
+  // its members are members[member_off[j] .. member_off[j+1]); the fp32 state
+  // of member r, query head h goes to entry
+  // ((part_base + r * max_depth + group_depth[j]) * Hkv + kvh) * g + h % g
+  const int32_t* group_start;
+  const int32_t* group_len;
+  const int32_t* group_depth;
+  const int32_t* member_off;
+  const int32_t* members;
+  float2* part_ml;  // (reference max in log2 units, row sum)
+  float* part_acc;  // unnormalised P.V rows, D floats each
+  int64_t part_base;
+  int32_t max_depth;
+  int32_t batch;  // member indices outside [0, batch) are skipped
 };
 
 // byte offset of 16-byte chunk `ci` (0..7) of row `row` inside one
@@ -128,8 +143,15 @@ SGL_DEV bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars, int* status) 
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
+// One CTA's work.  Extend mode: (request, KV head, two Q tiles of suffix
+// tokens), keys = the request's prefix from the pool, then its suffix,
+// causally; the normalised output is written as bf16.  Group mode: (shared
+// group, KV head, two Q tiles of the group's member requests), whose rows are
+// the members' decode queries and whose keys are the group's positions read
+// once from the first member's row; each row's fp32 softmax state (reference
+// max, row sum, unnormalised P.V) is written for the decode combine to merge.
+template <int D, bool kGroup>
+SGL_DEV void attend_tiles(const Params& p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -139,17 +161,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
   Bars* bars = reinterpret_cast<Bars*>(sKV + C::kStages * C::kTileBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // r: the request (extend mode) or the group (group mode); the "tokens" of
+  // the Q tiles are the request's suffix tokens or the group's members
   const int r = blockIdx.z, kvh = blockIdx.y;
-  const int e = p.extend_lens[r];
-  const int q0 = blockIdx.x * 2 * p.tpt;  // first suffix token of this CTA
-  if (q0 >= e) return;                    // nothing to do (uniform across the CTA)
-  const int pfx = p.prefix_lens[r];
+  const int mbeg = kGroup ? p.member_off[r] : 0;
+  const int e = kGroup ? p.member_off[r + 1] - mbeg : p.extend_lens[r];
+  const int q0 = blockIdx.x * 2 * p.tpt;                      // first token of this CTA
+  const int pfx = kGroup ? p.group_len[r] : p.prefix_lens[r];  // keys read from the pool
   const int q_end = min(e, q0 + 2 * p.tpt);
   const int nb_pre = (pfx + BN - 1) / BN;
-  const int nb = nb_pre + (q_end + BN - 1) / BN;
+  const int nb = nb_pre + (kGroup ? 0 : (q_end + BN - 1) / BN);
+  if (q0 >= e || nb <= 0) return;  // nothing to do (uniform across the CTA)
 
   // exclusive prefix sum of extend_lens: where request r's rows start
-  {
+  if constexpr (!kGroup) {
     int32_t part = 0;
     for (int i = tid; i < r; i += kThreads) part += p.extend_lens[i];
 #pragma unroll
@@ -179,8 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
   __syncthreads();
   tc_fence_after();
   int32_t off = 0;
+  if constexpr (!kGroup) {
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) off += bars->red[w];
+    for (int w = 0; w < kThreads / 32; ++w) off += bars->red[w];
+  }
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
 
@@ -305,7 +332,32 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
     *xchg_mine = l;
     named_bar_sync(pair_bar, 64);
     const float lrow = *xchg_mine + *xchg_other;
-    if (ok) {
+    if constexpr (kGroup) {
+      if (ok) {
+        tc_fence_after();
+        // this half writes columns [h*D/2, (h+1)*D/2) of the row's state
+        const int rm = row_valid ? p.members[mbeg + tok] : 0;
+        const int dep = p.group_depth[r];
+        const bool wr = row_valid && rm >= 0 && rm < p.batch && dep >= 0 && dep < p.max_depth;
+        const int64_t ent =
+            ((p.part_base + (int64_t)rm * p.max_depth + dep) * p.Hkv + kvh) * p.g + row % p.g;
+        float* dst = p.part_acc + ent * D + (D / 2) * h;
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) {
+          uint32_t o[32];
+          tmem_ld32(tO + (D / 2) * h + 32 * j, o);
+          tmem_wait_ld();
+          if (wr) {
+            float4* d4 = reinterpret_cast<float4*>(dst + 32 * j);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              d4[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                  __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+          }
+        }
+        if (wr && h == 0) p.part_ml[ent] = make_float2(m_ref, lrow);
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       // this half writes columns [h*D/2, (h+1)*D/2) of the output row
@@ -340,9 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
       for (int i = 0; i < kRowsPerThread; ++i) {
         const int row = rbase + kRowStep * i;
         const int tok = q0 + t * p.tpt + row / p.g;
-        const bool valid = row < p.rows_used && tok < e;
+        bool valid = row < p.rows_used && tok < e;
+        // the query row: suffix token off+tok, or member tok's decode query
+        int64_t qrow = valid ? (kGroup ? (int64_t)p.members[mbeg + tok] : (int64_t)(off + tok)) : 0;
+        if (kGroup && (qrow < 0 || qrow >= p.batch)) valid = false, qrow = 0;
         const __nv_bfloat16* src =
-            p.q + ((int64_t)(off + (valid ? tok : 0)) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + ci * 8;
+            p.q + (qrow * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + ci * 8;
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           cp_async_16(sQ_a + t * C::kTileBytes + c * C::kChunkBytes + sw128(row, ci),
@@ -352,7 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
     // each producer thread's arrival on q_full / kv_full fires when its own
     // copies have landed (no producer ever waits for its copies)
     cp_async_mbar_arrive(&bars->q_full);
-    const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride;
+    // group mode: the group's keys are read from its first member's row
+    const int32_t* rtt =
+        kGroup ? p.req_to_token + (int64_t)p.req_pool_idx[p.members[mbeg]] * p.rtt_stride +
+                     p.group_start[r]
+               : p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride;
     int32_t slot_cur[kRowsPerThread], slot_next[kRowsPerThread];
     auto load_slots = [&](int b, int32_t (&dst)[kRowsPerThread]) {
 #pragma unroll
@@ -495,6 +554,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
 }
 
 template <int D>
+__global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
+  attend_tiles<D, false>(p);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) cascade_group_kernel(Params p) {
+  attend_tiles<D, true>(p);
+}
+
+template <int D>
 sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = extend_kernel<D>;
@@ -508,7 +577,55 @@ sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
 }
 
+template <int D>
+sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members,
+                      cudaStream_t stream) {
+  auto kern = cascade_group_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<D>()) !=
+      cudaSuccess)
+    return SGL_ERR_CUDA;
+  const int per_cta = 2 * prm.tpt;
+  const unsigned gx = (unsigned)((max_members + per_cta - 1) / per_cta);
+  dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)n_groups);
+  kern<<<grid, kThreads, smem_bytes<D>(), stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
+}
+
 }  // namespace
+
+sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
+  if (a.n_groups == 0 || a.max_members == 0) return SGL_OK;
+  const int g = a.num_q_heads / a.num_kv_heads;
+  if (g < 1 || g > BM) return SGL_ERR_UNSUPPORTED;
+  if (a.n_groups > 65535 || a.num_kv_heads > 65535) return SGL_ERR_UNSUPPORTED;
+  Params prm = {};
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.pool_k = static_cast<const __nv_bfloat16*>(a.pool_k);
+  prm.pool_v = static_cast<const __nv_bfloat16*>(a.pool_v);
+  prm.req_to_token = a.req_to_token;
+  prm.rtt_stride = a.rtt_stride;
+  prm.req_pool_idx = a.req_pool_idx;
+  prm.Hq = a.num_q_heads;
+  prm.Hkv = a.num_kv_heads;
+  prm.g = g;
+  prm.tpt = BM / g;
+  prm.rows_used = prm.tpt * g;
+  prm.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  prm.status = a.status;
+  prm.group_start = a.group_start;
+  prm.group_len = a.group_len;
+  prm.group_depth = a.group_depth;
+  prm.member_off = a.member_off;
+  prm.members = a.members;
+  prm.part_ml = static_cast<float2*>(a.part_ml);
+  prm.part_acc = static_cast<float*>(a.part_acc);
+  prm.part_base = a.part_base;
+  prm.max_depth = a.max_depth;
+  prm.batch = a.batch;
+  if (a.head_dim == 128) return run_groups<128>(prm, a.n_groups, a.max_members, stream);
+  if (a.head_dim == 64) return run_groups<64>(prm, a.n_groups, a.max_members, stream);
+  return SGL_ERR_UNSUPPORTED;
+}
 
 size_t extend_workspace_bytes() { return 256; }
 
@@ -517,7 +634,7 @@ sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream) {
   const int g = a.num_q_heads / a.num_kv_heads;
   if (g < 1 || g > BM) return SGL_ERR_UNSUPPORTED;
   if (a.batch > 65535 || a.num_kv_heads > 65535) return SGL_ERR_UNSUPPORTED;
-  Params prm;
+  Params prm = {};
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
   prm.v_new = static_cast<const __nv_bfloat16*>(a.v_new);

@@ -29,10 +29,48 @@ struct DecodeArgs {
   size_t workspace_bytes;
   int32_t num_q_heads, num_kv_heads, head_dim;
   float sm_scale;
+  // cascade decode: shared-prefix groups (cascade == false: plain decode,
+  // the fields below are unused)
+  bool cascade = false;
+  const int32_t* group_start = nullptr;
+  const int32_t* group_len = nullptr;
+  const int32_t* group_depth = nullptr;
+  const int32_t* group_member_off = nullptr;
+  const int32_t* group_members = nullptr;
+  int32_t n_groups = 0, max_group_members = 0, max_depth = 0;
 };
+// bytes in front of a cascade workspace: word 0 is the bounded-wait status
+constexpr size_t kCascadeStatusBytes = 256;
 size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t num_q_heads,
-                              int32_t num_kv_heads, int32_t head_dim);
+                              int32_t num_kv_heads, int32_t head_dim, bool cascade = false,
+                              int32_t max_depth = 0);
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// The tensor-core pass of cascade decode: per (group, KV head, block of
+// members) the members' decode queries attend to the group's keys and every
+// row's fp32 softmax state goes to entry
+// ((part_base + member * max_depth + depth) * Hkv + kvh) * G + head % G.
+struct GroupArgs {
+  const void* q;
+  const void* pool_k;
+  const void* pool_v;
+  const int32_t* req_to_token;
+  int32_t rtt_stride;
+  const int32_t* req_pool_idx;
+  const int32_t* group_start;
+  const int32_t* group_len;
+  const int32_t* group_depth;
+  const int32_t* member_off;
+  const int32_t* members;
+  int32_t batch, n_groups, max_members, max_depth;
+  void* part_ml;   // float2 entries
+  void* part_acc;  // D floats per entry
+  int64_t part_base;
+  int* status;
+  int32_t num_q_heads, num_kv_heads, head_dim;
+  float sm_scale;
+};
+sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream);
 
 struct ExtendArgs {
   const void* q;

@@ -38,6 +38,17 @@ def decode_unique_bytes(req_to_token, req_pool_idx, seq_lens, num_q_heads, num_k
             + 2 * 2 * int(seq.size) * num_q_heads * head_dim)
 
 
+def cascade_decode_bytes(group_len, shared_lens, seq_lens, num_q_heads, num_kv_heads, head_dim) -> int:
+    """Like ``decode_bytes`` with every shared group's keys read once: the K+V
+    rows and slot ids of each group's keys and of each request's private tail
+    ``[shared_len, seq_len)``, plus q in and out."""
+    seq = np.asarray(seq_lens, dtype=np.int64)
+    tail = np.maximum(seq - np.asarray(shared_lens, dtype=np.int64), 0)
+    n_keys = int(np.sum(np.asarray(group_len, dtype=np.int64))) + int(tail.sum())
+    return (n_keys * (kv_bytes_per_token(num_kv_heads, head_dim) + 4)
+            + 2 * 2 * int(seq.size) * num_q_heads * head_dim)
+
+
 def extend_pairs(prefix_lens, extend_lens) -> int:
     """Unmasked (query, key) pairs per query head: suffix query i of a request
     with prefix p sees p + i + 1 keys, so the request adds e*p + e(e+1)/2."""

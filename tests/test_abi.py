@@ -110,6 +110,41 @@ def test_decode_validation_and_workspace_size(cuda_lib):
     assert B.extend_workspace_bytes(8, 16384, d) >= 16
 
 
+def test_cascade_validation_and_workspace_size(cuda_lib):
+    d = _dims(num_q_heads=16, num_kv_heads=4)
+    need = B.cascade_decode_workspace_bytes(8, 512, 3, d)
+    # status bytes in front, plus per-request group states
+    assert need >= B.decode_workspace_bytes(8, 512, d) + 256 + 8 * 3 * 16 * 128 * 4
+    f = cuda_lib.sgl_cascade_decode_attention
+
+    def call(**kw):
+        a = dict(q=FAKE, pk=FAKE, pv=FAKE, rtt=FAKE, rows=8, stride=512, rpi=FAKE, sl=FAKE, batch=8,
+                 max_s=512, gs=FAKE, gl=FAKE, gd=FAKE, mo=FAKE, mem=FAKE, n_groups=2, max_m=4,
+                 max_d=3, out=FAKE, ws=FAKE, wsb=need)
+        a.update(kw)
+        return f(a["q"], a["pk"], a["pv"], a["rtt"], a["rows"], a["stride"], a["rpi"], a["sl"],
+                 a["batch"], a["max_s"], a["gs"], a["gl"], a["gd"], a["mo"], a["mem"], a["n_groups"],
+                 a["max_m"], a["max_d"], a["out"], a["ws"], a["wsb"], ctypes.byref(d), None)
+    assert call(batch=0) == 0
+    assert call(n_groups=-1) == 1
+    assert call(gs=None) == 1
+    assert call(mem=None) == 1
+    assert call(max_d=0) == 1
+    assert call(max_m=0) == 1
+    assert call(n_groups=70000) == 2
+    assert call(ws=None) == 3
+    assert call(wsb=need - 1) == 3
+    assert call(q=MISALIGNED) == 1
+    # no groups: group arrays may be null
+    assert call(n_groups=0, gs=None, gl=None, gd=None, mo=None, mem=None, max_d=0, max_m=0,
+                ws=None) == 3
+    c = cuda_lib.sgl_check_cascade_groups
+    assert cuda_lib.sgl_check_cascade_scratch_bytes(8, 3) == 96
+    assert c(FAKE, 8, 512, FAKE, FAKE, 8, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 3, FAKE, 95, FAKE, None) == 3
+    assert c(FAKE, 8, 512, FAKE, FAKE, 8, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 3, None, 0, FAKE, None) == 0
+    assert c(FAKE, 8, 512, FAKE, FAKE, 8, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 3, FAKE, 96, None, None) == 1
+
+
 def test_check_calls_validate_on_host(cuda_lib):
     assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, None, None) == 1
     assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, FAKE, None) == 3  # bitmap small

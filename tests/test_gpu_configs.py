@@ -83,6 +83,22 @@ def test_tree_of_thought_decode_full():
     _check_store(run, w.decode[-1])
 
 
+def test_tree_of_thought_cascade_full():
+    """The tree workload through cascade decode, with the shared levels read
+    once per group; sampled leaves against the oracle's plain decode."""
+    from test_gpu_cascade import cascade
+    w = W.tree_of_thought_decode()
+    run = Run(w)
+    cg = W.tree_groups(w)
+    assert cg.n_groups == 84 and cg.max_members == 64
+    outs = [cascade(run, W.tree_groups(w, s), step=s) for s in range(len(w.decode))]
+    for s in (0, 8, len(w.decode) - 1):
+        _check_all_finite(outs[s], f"cascade step {s}")
+        reqs = _sample_requests(w.decode[s].seq_lens, 5, 20 + s)
+        want = oracle_decode(w, s, requests=reqs, pool=w.pool_view(decode_steps=s + 1))
+        assert_close(outs[s][reqs], want, f"tree cascade step {s}")
+
+
 def test_chunked_prefill_mix_full():
     w = W.chunked_prefill_mix()
     run = Run(w)
