@@ -319,13 +319,15 @@ decode_split_kernel(Params p) {
         for (int v = 0; v < L::kVecs; ++v)
           bf16x8_to_f32(*reinterpret_cast<const uint4*>(ks + tok * L::kRowBytes + 2 * L::elem(v, li)),
                         &kf[v * 8]);
+        // q.k and p.v on the packed fp32 pipe (two lanes of FMA per instruction)
         float s[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float a = 0.f;
+          float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < EL; ++e) a = fmaf(qf[h][e], kf[e], a);
-          s[h] = a;
+          for (int e = 0; e < EL; e += 2)
+            a = ffma2(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+          s[h] = a.x + a.y;
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -358,7 +360,12 @@ decode_split_kernel(Params p) {
           const float pw = valid ? ex2(s[h] - m[h]) : 0.f;
           l[h] += pw;
 #pragma unroll
-          for (int e = 0; e < EL; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+          for (int e = 0; e < EL; e += 2) {
+            const float2 a = ffma2(make_float2(pw, pw), make_float2(vf[e], vf[e + 1]),
+                                   make_float2(acc[h][e], acc[h][e + 1]));
+            acc[h][e] = a.x;
+            acc[h][e + 1] = a.y;
+          }
         }
       }
     }
