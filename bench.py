@@ -333,6 +333,23 @@ def work_of(w: W.Workload, groups=()):
                 decode_read_once_bytes=dec_unique, store_bytes=st_bytes)
 
 
+def capture_step(step):
+    """One step recorded as a CUDA graph (every launch of the step, replayed
+    with one call, as a serving loop replays its decode step)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.run()
+    torch.cuda.synchronize()
+    return g
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -352,20 +369,32 @@ def gpu_arm(args):
         flush.zero_()
     torch.cuda.synchronize()
 
+    graph = capture_step(step) if args.graph == "on" else None
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     launches = 0
     with ClockSampler(local) as clocks:
         wall0 = time.perf_counter()
+        if graph is not None:
+            # the headline: the step replayed as one CUDA graph
+            for k in range(args.steps):
+                gevs[k][0].record()
+                graph.replay()
+                gevs[k][1].record()
+                launches += step.launches
+                flush.zero_()                   # outside the events: L2 cold for every step
+        # per-kernel breakdown: the same step launched eagerly between events
         for k in range(args.steps):
             step.run(evs[k])
             launches += step.launches
-            flush.zero_()                       # outside the events: L2 cold for every step
+            flush.zero_()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier()
-    t_step = [evs[k][0].elapsed_time(evs[k][3]) for k in range(args.steps)]
+    t_eager = [evs[k][0].elapsed_time(evs[k][3]) for k in range(args.steps)]
+    t_step = [gevs[k][0].elapsed_time(gevs[k][1]) for k in range(args.steps)] if graph is not None else t_eager
     t_store = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
     t_ext = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
     t_dec = [evs[k][2].elapsed_time(evs[k][3]) for k in range(args.steps)]
@@ -379,6 +408,7 @@ def gpu_arm(args):
     # an H2D stream, results on a D2H stream, and events order buffer reuse.
     bufs = [step, step.twin()]
     io = [b.host_io() for b in bufs]
+    graphs = [graph, capture_step(bufs[1])] if graph is not None else None
     h2d_bytes = sum(x.numel() * x.element_size() for x, _ in io[0][0])
     d2h_bytes = sum(x.numel() * x.element_size() for x, _ in io[0][1])
     e_steps = max(4, min(args.steps, 40))
@@ -402,7 +432,10 @@ def gpu_arm(args):
             compute.wait_event(inp)
             if k >= 2:
                 compute.wait_event(got[k - 2])         # step k-2's results are out
-            b.run()
+            if graphs is not None:
+                graphs[k % 2].replay()
+            else:
+                b.run()
             done[k].record(compute)
             flush.zero_()
             with torch.cuda.stream(d2h_s):
@@ -470,6 +503,7 @@ def gpu_arm(args):
                    "decode_requests": int(sum(b.q.shape[0] for b in w.decode)),
                    "query_tokens_per_step": int(step.tokens), "parallelism": f"replicas{world}",
                    "decode_path": ("cascade" if step.cascade else "plain") if w.decode else None,
+                   "launch": "cuda_graph" if graph is not None else "eager",
                    "l2": "flushed between steps (256 MiB write)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_bytes),
                 "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e_ms, 4),
@@ -478,6 +512,7 @@ def gpu_arm(args):
         "gpu_launches": int(launches),
         "roofline": roof,
         "kernels": kernels,
+        "eager_ms_per_step": round(statistics.mean(t_eager), 4),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 3),
     }
@@ -591,6 +626,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOAD_NAMES))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", choices=["on", "off"], default="on",
+                    help="time the step replayed as one CUDA graph (per-kernel times stay eager)")
     ap.add_argument("--cascade", choices=["auto", "on", "off"], default="auto",
                     help="decode through shared-prefix groups (auto: when the batch shares prefixes)")
     ap.add_argument("--small", action="store_true",

@@ -491,20 +491,14 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
   static_assert(kWarps * G * (D + 2) * sizeof(float) <= (size_t)kStages * 2 * kTile * D * 2,
                 "reduction scratch must fit in the ring");
   auto kern = decode_split_kernel<D, G, LPT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return SGL_ERR_CUDA;
+  const int blocks_per_sm = kernel_blocks_per_sm<decode_split_kernel<D, G, LPT>>((int)smem, kThreads);
+  if (blocks_per_sm < 0) return SGL_ERR_CUDA;
   decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.Hkv, prm.ws,
                                              gr);
   if (ga != nullptr) {
     const sgl_status st = launch_cascade_groups(*ga, stream);
     if (st != SGL_OK) return st;
   }
-  int blocks_per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, kThreads, smem) !=
-          cudaSuccess ||
-      blocks_per_sm < 1)
-    blocks_per_sm = 1;
   // two waves of CTAs (every CTA keeps taking items while any are left)
   int64_t gx = ((int64_t)2 * blocks_per_sm * num_sms() + prm.Hkv - 1) / prm.Hkv;
   if (gx > max_items) gx = max_items;

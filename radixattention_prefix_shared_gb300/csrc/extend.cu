@@ -567,9 +567,7 @@ template <int D>
 sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = extend_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<D>()) !=
-      cudaSuccess)
-    return SGL_ERR_CUDA;
+  if (kernel_blocks_per_sm<extend_kernel<D>>(smem_bytes<D>(), kThreads) < 0) return SGL_ERR_CUDA;
   const int per_cta = 2 * prm.tpt;
   const unsigned gx = (unsigned)((max_extend + per_cta - 1) / per_cta);
   dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)batch);
@@ -581,8 +579,7 @@ template <int D>
 sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members,
                       cudaStream_t stream) {
   auto kern = cascade_group_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<D>()) !=
-      cudaSuccess)
+  if (kernel_blocks_per_sm<cascade_group_kernel<D>>(smem_bytes<D>(), kThreads) < 0)
     return SGL_ERR_CUDA;
   const int per_cta = 2 * prm.tpt;
   const unsigned gx = (unsigned)((max_members + per_cta - 1) / per_cta);

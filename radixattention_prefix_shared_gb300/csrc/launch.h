@@ -5,12 +5,38 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/sgl_attn.h"
 
 namespace sgl {
 
 // SM count of the current device (cached per device).
 int num_sms();
+
+// Raises kernel Kern's dynamic shared memory limit to `smem` bytes and returns
+// how many of its blocks of `threads` fit on one SM (>= 1), or -1 on a CUDA
+// error.  Done once per device and kernel: later calls (including calls made
+// while a stream is being captured into a CUDA graph) only read the cache.
+template <auto Kern>
+int kernel_blocks_per_sm(int smem, int threads) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  if (cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kern, threads, (size_t)smem) != cudaSuccess)
+    return -1;
+  if (b < 1) b = 1;
+  if (cached) cache[dev].store(b, std::memory_order_relaxed);
+  return b;
+}
 
 sgl_status launch_store_kv(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
                            void* pool_k, void* pool_v, int32_t row_bytes, cudaStream_t stream);
