@@ -23,6 +23,10 @@ What it computes, and where the pages fix it:
     request's private tail, merged exactly; shared prefixes are identical
     slot numbers in the rows ("Inside SGLang", Step 3: Paged KV and the
     kernels that read it).
+  * FP8 KV pool (``oracle.fp8``): e4m3 codes with one scale per tensor,
+    quantised from the float32 quotient x / scale, decode over the
+    dequantised rows -- "Inside SGLang", Step 6 (Decide how much memory
+    becomes KV cache: --kv-cache-dtype fp8_e4m3, scales from the checkpoint).
 All arithmetic is float64.  Every function is pinned by ``tests/test_oracle.py``
 against closed forms, a library routine (full causal attention recomputed from
 scratch), invariants and brute force; see that file for the list.
@@ -39,3 +43,4 @@ from .attention import (  # noqa: F401
     merge_states,
     cascade_decode_attention,
 )
+from . import fp8  # noqa: F401
