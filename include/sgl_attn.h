@@ -229,6 +229,36 @@ sgl_status sgl_cascade_decode_attention(
     int32_t n_groups, int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
     size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream);
 
+/*
+ * FP8 KV pool ("Inside SGLang", Step 6: Decide how much memory becomes KV
+ * cache -- with --kv-cache-dtype fp8_e4m3 each token's K and V take half the
+ * bytes; the attention kernels read FP8 directly, and K and V carry one scale
+ * each, from the checkpoint, 1.0 when missing).
+ *
+ * Pool rows hold e4m3 codes (uint8 [S, Hkv, D]: 1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, subnormals, no infinities, largest finite 448); a
+ * code c of pool_k stands for the value e4m3(c) * k_scale (pool_v: v_scale).
+ *
+ * sgl_store_kv_fp8 -- pool_k[slots[i]] = e4m3(k_new[i] / k_scale), likewise
+ *   V: the quotient in IEEE float32, rounded to e4m3 to nearest (ties to
+ *   even), saturating to +-448.  k_new, v_new bf16 [n, Hkv, D]; slots as in
+ *   sgl_store_kv; scales finite and > 0 (else SGL_ERR_INVALID_ARG).
+ * sgl_decode_attention_fp8 -- sgl_decode_attention over an e4m3 pool: the
+ *   keys and values are code * scale; q, out and the workspace as there
+ *   (sgl_decode_workspace_bytes).  The K scale is folded into the query and
+ *   the V scale into the output; accumulation is fp32.
+ */
+sgl_status sgl_store_kv_fp8(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
+                            void* pool_k, void* pool_v, float k_scale, float v_scale,
+                            const sgl_attn_dims* dims, sgl_stream_t stream);
+sgl_status sgl_decode_attention_fp8(const void* q, const void* pool_k, const void* pool_v,
+                                    float k_scale, float v_scale, const int32_t* req_to_token,
+                                    int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* seq_lens,
+                                    int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                                    size_t workspace_bytes, const sgl_attn_dims* dims,
+                                    sgl_stream_t stream);
+
 /* Workspace sizes (host only; no device call). */
 size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims);
 size_t sgl_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, const sgl_attn_dims* dims);

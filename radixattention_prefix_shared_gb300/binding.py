@@ -55,6 +55,11 @@ _SIGS = {
                                                     c_i32, c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims),
                                                     c_vp]),
     "sgl_cascade_decode_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, _P(sgl_attn_dims)]),
+    "sgl_store_kv_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_f32, c_f32,
+                                        _P(sgl_attn_dims), c_vp]),
+    "sgl_decode_attention_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_f32, c_f32, c_vp, c_i32, c_i32, c_vp,
+                                                c_vp, c_i32, c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims),
+                                                c_vp]),
     "sgl_check_cascade_scratch_bytes": (c_size, [c_i32, c_i32]),
     "sgl_check_cascade_groups": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
                                                 c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_size, c_vp,
@@ -245,3 +250,31 @@ def sgl_check_cascade_groups(req_to_token, req_pool_idx, seq_lens, group_start, 
         _ptr(seq_lens), B, _ptr(group_start), _ptr(group_len), _ptr(group_depth), _ptr(group_member_off),
         _ptr(group_members), int(group_start.shape[0]), int(max_group_members), int(max_depth),
         _ptr(scratch), int(scratch.numel()), _ptr(d_error), _stream(stream)))
+
+
+# ----------------------------------------------------------------- FP8 pool
+
+def sgl_store_kv_fp8(k_new, v_new, slots, pool_k, pool_v, k_scale, v_scale, stream=None):
+    """pool[slots[i]] = e4m3(new[i] / scale) for K and V (pools: torch.uint8 [S, Hkv, D])."""
+    d = make_dims(pool_k.shape[1], pool_k.shape[1], pool_k.shape[2], pool_k.shape[0])
+    _check("sgl_store_kv_fp8", lib().sgl_store_kv_fp8(
+        _ptr(k_new), _ptr(v_new), _ptr(slots), int(slots.shape[0]), _ptr(pool_k), _ptr(pool_v),
+        float(k_scale), float(v_scale), ctypes.byref(d), _stream(stream)))
+
+
+def sgl_decode_attention_fp8(q, pool_k, pool_v, k_scale, v_scale, req_to_token, req_pool_idx, seq_lens,
+                             out=None, *, max_seq_len, workspace=None, sm_scale=0.0, stream=None):
+    """Decode attention over an e4m3 pool (values are code * scale)."""
+    import torch
+    d = _dims_for(q, pool_k, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    B = int(q.shape[0])
+    if workspace is None:
+        workspace = new_workspace(decode_workspace_bytes(B, max_seq_len, d), q.device)
+    _check("sgl_decode_attention_fp8", lib().sgl_decode_attention_fp8(
+        _ptr(q), _ptr(pool_k), _ptr(pool_v), float(k_scale), float(v_scale), _ptr(req_to_token),
+        int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(seq_lens), B,
+        int(max_seq_len), _ptr(out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        ctypes.byref(d), _stream(stream)))
+    return out

@@ -24,6 +24,8 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool valid_kv_scale(float s) { return s > 0.f && !isinf(s) && !isnan(s); }
+
 // Validates dims and fills the effective scale; returns SGL_OK or an error.
 sgl_status check_dims(const sgl_attn_dims* d, float* scale) {
   if (d == nullptr) return SGL_ERR_INVALID_ARG;
@@ -243,6 +245,23 @@ sgl_status sgl_store_kv(const void* k_new, const void* v_new, const int32_t* slo
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+sgl_status sgl_store_kv_fp8(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
+                            void* pool_k, void* pool_v, float k_scale, float v_scale,
+                            const sgl_attn_dims* dims, sgl_stream_t stream) {
+  float scale;
+  sgl_status st = check_dims(dims, &scale);
+  if (st != SGL_OK) return st;
+  if (n < 0 || !valid_kv_scale(k_scale) || !valid_kv_scale(v_scale)) return SGL_ERR_INVALID_ARG;
+  if (n == 0) return SGL_OK;
+  if (!k_new || !v_new || !slots || !pool_k || !pool_v) return SGL_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) || !aligned16(pool_v))
+    return SGL_ERR_INVALID_ARG;
+  if ((int64_t)n > dims->pool_size) return SGL_ERR_INVALID_ARG;
+  return launch_store_kv_fp8(k_new, v_new, slots, n, pool_k, pool_v,
+                             dims->num_kv_heads * dims->head_dim, k_scale, v_scale,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims) {
   (void)batch;
   (void)total_extend;
@@ -310,12 +329,44 @@ sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_
   return launch_extend(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, bool kv_fp8,
+                        float k_scale, float v_scale, const int32_t* req_to_token, int32_t rtt_rows,
+                        int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+                        int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream);
+}  // namespace
+
 sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* pool_v,
                                 const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
                                 const int32_t* req_pool_idx, const int32_t* seq_lens,
                                 int32_t batch, int32_t max_seq_len, void* out, void* workspace,
                                 size_t workspace_bytes, const sgl_attn_dims* dims,
                                 sgl_stream_t stream) {
+  return decode_entry(q, pool_k, pool_v, false, 1.f, 1.f, req_to_token, rtt_rows, rtt_stride,
+                      req_pool_idx, seq_lens, batch, max_seq_len, out, workspace, workspace_bytes,
+                      dims, stream);
+}
+
+sgl_status sgl_decode_attention_fp8(const void* q, const void* pool_k, const void* pool_v,
+                                    float k_scale, float v_scale, const int32_t* req_to_token,
+                                    int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* seq_lens,
+                                    int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                                    size_t workspace_bytes, const sgl_attn_dims* dims,
+                                    sgl_stream_t stream) {
+  if (!valid_kv_scale(k_scale) || !valid_kv_scale(v_scale)) return SGL_ERR_INVALID_ARG;
+  return decode_entry(q, pool_k, pool_v, true, k_scale, v_scale, req_to_token, rtt_rows,
+                      rtt_stride, req_pool_idx, seq_lens, batch, max_seq_len, out, workspace,
+                      workspace_bytes, dims, stream);
+}
+
+namespace {
+sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, bool kv_fp8,
+                        float k_scale, float v_scale, const int32_t* req_to_token, int32_t rtt_rows,
+                        int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+                        int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
   float scale;
   sgl_status st = check_dims(dims, &scale);
   if (st != SGL_OK) return st;
@@ -347,8 +398,12 @@ sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* p
   a.num_kv_heads = dims->num_kv_heads;
   a.head_dim = dims->head_dim;
   a.sm_scale = scale;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
+}  // namespace
 
 sgl_status sgl_cascade_decode_attention(
     const void* q, const void* pool_k, const void* pool_v, const int32_t* req_to_token,

@@ -14,7 +14,7 @@
 //                 per-KV-head counter; y: KV head) runs
 //                 each item: the slot indices go to shared memory, K and V
 //                 rows of the KV head are gathered by 16-byte cp.async into a
-//                 kStages-deep ring of kTile-key tiles, and the query heads of
+//                 kStages-deep ring of tiles (32 bf16 or 64 e4m3 keys), and the query heads of
 //                 the group share every loaded row.  LPT (8 or 16) lanes own one
 //                 key, each lane a slice of the head dim; every lane group keeps its own
 //                 fp32 online-softmax state (max, sum, weighted V sum) with
@@ -31,6 +31,8 @@
 // Scores are kept in the log2 domain (scale * log2(e) folded into q) and the
 // running max is only moved when a score exceeds it by more than 2^8, which
 // keeps every exponentiated weight <= 256 in fp32 and makes rescaling rare.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -48,7 +50,7 @@ namespace {
 #define SGL_DECODE_STAGES 4
 #endif
 constexpr int kChunk = SGL_DECODE_CHUNK;  // keys per work item
-constexpr int kTile = SGL_DECODE_TILE;    // keys per pipeline stage
+constexpr int kTileBf16 = SGL_DECODE_TILE;  // bf16 keys per pipeline stage (twice as many e4m3)
 constexpr int kStages = SGL_DECODE_STAGES;  // ring depth
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
@@ -114,15 +116,16 @@ inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G
 
 struct Params {
   const __nv_bfloat16* q;
-  const __nv_bfloat16* pool_k;
-  const __nv_bfloat16* pool_v;
+  const uint8_t* pool_k;  // [S, Hkv, D] rows of bf16 or e4m3 values
+  const uint8_t* pool_v;
   const int32_t* req_to_token;
   int64_t rtt_stride;
   const int32_t* req_pool_idx;
   const int32_t* seq_lens;
   __nv_bfloat16* out;
   int32_t batch, Hq, Hkv;
-  float scale_log2;
+  float scale_log2;  // softmax scale * log2(e) * K scale (1 for a bf16 pool)
+  float v_scale;     // V scale of an e4m3 pool (1 for bf16), applied to the output
   Ws ws;
   int64_t group_base;  // first partial entry of the group states (= max_items)
   int32_t max_depth;   // group states per request (cascade), else 0
@@ -198,28 +201,68 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
 
 // ---------------------------------------------------------------- split
 
-// LPT lanes own one key; each lane holds D/LPT consecutive-in-16-byte-vectors
-// elements of the head dim.  LPT = 8 for small head groups, 16 when G*D is
-// large (keeps the per-lane query and accumulator registers bounded).
-template <int D, int LPT>
+// LPT lanes own one key; each lane holds D/LPT elements of the head dim, in
+// chunks of at most 16 bytes of the stored row (8 bf16 or 16 e4m3 values);
+// the LPT lanes' chunks are contiguous, so a warp's loads are coalesced.
+// LPT = 8 for small head groups, 16 when G*D is large (keeps the per-lane
+// query and accumulator registers bounded).  KV is the pool's element type:
+// __nv_bfloat16, or uint8_t holding e4m3 codes.
+template <int D, int LPT, typename KV>
 struct Lane {
-  static constexpr int kVecs = D / (8 * LPT);  // 16-byte vectors per lane per row
-  static constexpr int kElems = kVecs * 8;     // elements per lane
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kRowVecs = D / 8;       // 16-byte vectors per row
-  static constexpr int kGroups = 32 / LPT;     // keys per warp instruction
-  // element offset of vector v of lane li
-  static __device__ __forceinline__ int elem(int v, int li) { return v * (8 * LPT) + li * 8; }
+  static constexpr int kBytes = (int)sizeof(KV);
+  static constexpr int kRowBytes = D * kBytes;
+  static constexpr int kRowVecs = kRowBytes / 16;  // 16-byte vectors per row
+  static constexpr int kElems = D / LPT;           // elements per lane
+  static constexpr int kChunkElems = (16 / kBytes) < kElems ? (16 / kBytes) : kElems;
+  static constexpr int kChunks = kElems / kChunkElems;
+  static constexpr int kGroups = 32 / LPT;         // keys per warp instruction
+  // element offset of chunk c of lane li
+  static __device__ __forceinline__ int elem(int c, int li) {
+    return c * (kChunkElems * LPT) + li * kChunkElems;
+  }
 };
+
+// n stored values of type KV at p -> n floats (e4m3 codes are exact in float)
+template <typename KV, int N>
+SGL_DEV void load_row_chunk(const uint8_t* p, float* f) {
+  if constexpr (sizeof(KV) == 2) {
+    static_assert(N == 8, "one 16-byte vector of bf16");
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(p), f);
+  } else {
+    static_assert(N == 8 || N == 16, "8 or 16 e4m3 codes");
+    uint32_t w[N / 4];
+    if constexpr (N == 16) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p);
+      w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      w[0] = v.x, w[1] = v.y;
+    }
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+            (__nv_fp8x2_storage_t)(w[i] >> (16 * h)), __NV_E4M3);
+        const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&r));
+        f[4 * i + 2 * h] = x.x;
+        f[4 * i + 2 * h + 1] = x.y;
+      }
+    }
+  }
+}
 
 template <int D, int G, int LPT>
 constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
 
-template <int D, int G, int LPT>
+template <int D, int G, int LPT, typename KV>
 __global__ void __launch_bounds__(kThreads, (min_blocks<D, G, LPT>()))
 decode_split_kernel(Params p) {
-  using L = Lane<D, LPT>;
+  using L = Lane<D, LPT, KV>;
   constexpr int EL = L::kElems;
+  constexpr int CE = L::kChunkElems;
+  // a stage holds the same bytes for either pool type (64 e4m3 keys or 32 bf16)
+  constexpr int kTile = SGL_DECODE_TILE * 2 / L::kBytes;  // keys per pipeline stage
   constexpr int kTileBytes = kTile * L::kRowBytes;         // one K or V tile
   constexpr int kStageBytes = 2 * kTileBytes;              // K then V
   extern __shared__ __align__(128) uint8_t smem[];
@@ -261,18 +304,20 @@ decode_split_kernel(Params p) {
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int v = 0; v < L::kVecs; ++v) {
-          uint4 raw = *reinterpret_cast<const uint4*>(qb + h * D + L::elem(v, li));
-          bf16x8_to_f32(raw, &qf[h][v * 8]);
+        for (int c = 0; c < L::kChunks; ++c)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) qf[h][v * 8 + e] *= p.scale_log2;
-        }
+          for (int u = 0; u < CE; u += 8) {
+            uint4 raw = *reinterpret_cast<const uint4*>(qb + h * D + L::elem(c, li) + u);
+            bf16x8_to_f32(raw, &qf[h][c * CE + u]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[h][c * CE + u + e] *= p.scale_log2;
+          }
     }
     __syncthreads();  // slots visible; previous item's reduction scratch free
 
     const int n_tiles = (n + kTile - 1) / kTile;
-    const __nv_bfloat16* kbase = p.pool_k + (int64_t)kvh * D;
-    const __nv_bfloat16* vbase = p.pool_v + (int64_t)kvh * D;
+    const uint8_t* kbase = p.pool_k + (int64_t)kvh * L::kRowBytes;
+    const uint8_t* vbase = p.pool_v + (int64_t)kvh * L::kRowBytes;
     auto issue = [&](int tile, int stage) {
       const uint32_t st = ring + stage * kStageBytes;
       constexpr int kRowsPerPass = kThreads / L::kRowVecs;
@@ -284,8 +329,8 @@ decode_split_kernel(Params p) {
         const bool ok = j < n;
         const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv : 0;
         const uint32_t d = st + tok * L::kRowBytes + vec * 16;
-        cp_async_16(d, kbase + row * D + vec * 8, ok ? 16u : 0u);
-        cp_async_16(d + kTileBytes, vbase + row * D + vec * 8, ok ? 16u : 0u);
+        cp_async_16(d, kbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
+        cp_async_16(d + kTileBytes, vbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
       }
     };
 #pragma unroll
@@ -316,9 +361,8 @@ decode_split_kernel(Params p) {
         const bool valid = k * kTile + tok < n;
         float kf[EL];
 #pragma unroll
-        for (int v = 0; v < L::kVecs; ++v)
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(ks + tok * L::kRowBytes + 2 * L::elem(v, li)),
-                        &kf[v * 8]);
+        for (int c = 0; c < L::kChunks; ++c)
+          load_row_chunk<KV, CE>(ks + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &kf[c * CE]);
         // q.k and p.v on the packed fp32 pipe (two lanes of FMA per instruction)
         float s[G];
 #pragma unroll
@@ -352,9 +396,8 @@ decode_split_kernel(Params p) {
         }
         float vf[EL];
 #pragma unroll
-        for (int v = 0; v < L::kVecs; ++v)
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vs + tok * L::kRowBytes + 2 * L::elem(v, li)),
-                        &vf[v * 8]);
+        for (int c = 0; c < L::kChunks; ++c)
+          load_row_chunk<KV, CE>(vs + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &vf[c * CE]);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float pw = valid ? ex2(s[h] - m[h]) : 0.f;
@@ -399,10 +442,10 @@ decode_split_kernel(Params p) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
-        for (int v = 0; v < L::kVecs; ++v)
+        for (int c = 0; c < L::kChunks; ++c)
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_acc[(warp * G + h) * D + L::elem(v, li) + e] = acc[h][v * 8 + e];
+          for (int e = 0; e < CE; ++e)
+            red_acc[(warp * G + h) * D + L::elem(c, li) + e] = acc[h][c * CE + e];
         if (li == 0) {
           red_m[warp * G + h] = m[h];
           red_l[warp * G + h] = l[h];
@@ -425,7 +468,7 @@ decode_split_kernel(Params p) {
         A += red_acc[(w * G + h) * D + d] * f;
       }
       if (single) {
-        p.out[((int64_t)r * p.Hq + (int64_t)kvh * G + h) * D + d] = __float2bfloat16_rn(A / Ls);
+        p.out[((int64_t)r * p.Hq + (int64_t)kvh * G + h) * D + d] = __float2bfloat16_rn(A * (p.v_scale / Ls));
       } else {
         const int64_t slot = ((int64_t)item * p.Hkv + kvh) * G + h;
         p.ws.part_acc[slot * D + d] = A;
@@ -477,21 +520,21 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(Params p) {
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = fmaf(f, a[lane + 32 * e], acc[e]);
   }
-  const float inv = 1.f / Ls;
+  const float inv = p.v_scale / Ls;
   __nv_bfloat16* o = p.out + ((int64_t)r * p.Hq + h) * D;
 #pragma unroll
   for (int e = 0; e < E; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
 }
 
-template <int D, int G>
+template <int D, int G, typename KV>
 sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const GroupArgs* ga,
                cudaStream_t stream) {
   constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
-  constexpr size_t smem = (size_t)kStages * 2 * kTile * D * 2 + kChunk * sizeof(int32_t);
-  static_assert(kWarps * G * (D + 2) * sizeof(float) <= (size_t)kStages * 2 * kTile * D * 2,
-                "reduction scratch must fit in the ring");
-  auto kern = decode_split_kernel<D, G, LPT>;
-  const int blocks_per_sm = kernel_blocks_per_sm<decode_split_kernel<D, G, LPT>>((int)smem, kThreads);
+  constexpr size_t kRing = (size_t)kStages * 2 * kTileBf16 * D * 2;  // same bytes for e4m3
+  constexpr size_t smem = kRing + kChunk * sizeof(int32_t);
+  static_assert(kWarps * G * (D + 2) * sizeof(float) <= kRing, "reduction scratch must fit in the ring");
+  auto kern = decode_split_kernel<D, G, LPT, KV>;
+  const int blocks_per_sm = kernel_blocks_per_sm<decode_split_kernel<D, G, LPT, KV>>((int)smem, kThreads);
   if (blocks_per_sm < 0) return SGL_ERR_CUDA;
   decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.Hkv, prm.ws,
                                              gr);
@@ -509,14 +552,14 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
 }
 
-template <int D>
+template <int D, typename KV>
 sgl_status run_g(int G, const Params& prm, int64_t max_items, const Groups& gr,
                  const GroupArgs* ga, cudaStream_t stream) {
   switch (G) {
-    case 1: return run<D, 1>(prm, max_items, gr, ga, stream);
-    case 2: return run<D, 2>(prm, max_items, gr, ga, stream);
-    case 4: return run<D, 4>(prm, max_items, gr, ga, stream);
-    case 8: return run<D, 8>(prm, max_items, gr, ga, stream);
+    case 1: return run<D, 1, KV>(prm, max_items, gr, ga, stream);
+    case 2: return run<D, 2, KV>(prm, max_items, gr, ga, stream);
+    case 4: return run<D, 4, KV>(prm, max_items, gr, ga, stream);
+    case 8: return run<D, 8, KV>(prm, max_items, gr, ga, stream);
     default: return SGL_ERR_UNSUPPORTED;
   }
 }
@@ -538,8 +581,8 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
-  prm.pool_k = static_cast<const __nv_bfloat16*>(a.pool_k);
-  prm.pool_v = static_cast<const __nv_bfloat16*>(a.pool_v);
+  prm.pool_k = static_cast<const uint8_t*>(a.pool_k);
+  prm.pool_v = static_cast<const uint8_t*>(a.pool_v);
   prm.req_to_token = a.req_to_token;
   prm.rtt_stride = a.rtt_stride;
   prm.req_pool_idx = a.req_pool_idx;
@@ -548,7 +591,10 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.batch = a.batch;
   prm.Hq = a.num_q_heads;
   prm.Hkv = a.num_kv_heads;
-  prm.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  // the K scale of an e4m3 pool folds into the query, the V scale into the output
+  prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale : 1.f);
+  prm.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
+  if (a.kv_fp8 && a.cascade) return SGL_ERR_UNSUPPORTED;
   // cascade: word 0 of the workspace is the group pass's status; the decode
   // scratch follows the status bytes
   const size_t head = a.cascade ? kCascadeStatusBytes : 0;
@@ -591,8 +637,13 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     ga.sm_scale = a.sm_scale;
   }
   const GroupArgs* gp = groups ? &ga : nullptr;
-  if (a.head_dim == 128) return run_g<128>(G, prm, max_items, gr, gp, stream);
-  if (a.head_dim == 64) return run_g<64>(G, prm, max_items, gr, gp, stream);
+  if (a.kv_fp8) {
+    if (a.head_dim == 128) return run_g<128, uint8_t>(G, prm, max_items, gr, gp, stream);
+    if (a.head_dim == 64) return run_g<64, uint8_t>(G, prm, max_items, gr, gp, stream);
+    return SGL_ERR_UNSUPPORTED;
+  }
+  if (a.head_dim == 128) return run_g<128, __nv_bfloat16>(G, prm, max_items, gr, gp, stream);
+  if (a.head_dim == 64) return run_g<64, __nv_bfloat16>(G, prm, max_items, gr, gp, stream);
   return SGL_ERR_UNSUPPORTED;
 }
 

@@ -40,6 +40,10 @@ int kernel_blocks_per_sm(int smem, int threads) {
 
 sgl_status launch_store_kv(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
                            void* pool_k, void* pool_v, int32_t row_bytes, cudaStream_t stream);
+// bf16 rows of row_elems values quantised into e4m3 pool rows
+sgl_status launch_store_kv_fp8(const void* k_new, const void* v_new, const int32_t* slots,
+                               int32_t n, void* pool_k, void* pool_v, int32_t row_elems,
+                               float k_scale, float v_scale, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;
@@ -64,6 +68,9 @@ struct DecodeArgs {
   const int32_t* group_member_off = nullptr;
   const int32_t* group_members = nullptr;
   int32_t n_groups = 0, max_group_members = 0, max_depth = 0;
+  // e4m3 pool (kv_fp8): pool rows hold codes; K/V values are code * scale
+  bool kv_fp8 = false;
+  float k_scale = 1.f, v_scale = 1.f;
 };
 // bytes in front of a cascade workspace: word 0 is the bounded-wait status
 constexpr size_t kCascadeStatusBytes = 256;

@@ -145,6 +145,24 @@ def test_cascade_validation_and_workspace_size(cuda_lib):
     assert c(FAKE, 8, 512, FAKE, FAKE, 8, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 3, FAKE, 96, None, None) == 1
 
 
+def test_fp8_validation(cuda_lib):
+    d = _dims()
+    f = cuda_lib.sgl_store_kv_fp8
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 1.0, 0.0, ctypes.byref(d), None) == 1      # v_scale 0
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, float("nan"), 1.0, ctypes.byref(d), None) == 1
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, float("inf"), 1.0, ctypes.byref(d), None) == 1
+    assert f(None, None, None, 0, None, None, 1.0, 1.0, ctypes.byref(d), None) == 0
+    assert f(MISALIGNED, FAKE, FAKE, 4, FAKE, FAKE, 1.0, 1.0, ctypes.byref(d), None) == 1
+    g = cuda_lib.sgl_decode_attention_fp8
+    need = B.decode_workspace_bytes(2, 64, d)
+    assert g(FAKE, FAKE, FAKE, -1.0, 1.0, FAKE, 4, 64, FAKE, FAKE, 2, 64, FAKE, FAKE, need,
+             ctypes.byref(d), None) == 1
+    assert g(FAKE, FAKE, FAKE, 1.0, 1.0, FAKE, 4, 64, FAKE, FAKE, 2, 64, FAKE, None, need,
+             ctypes.byref(d), None) == 3
+    assert g(FAKE, FAKE, FAKE, 1.0, 1.0, FAKE, 4, 64, FAKE, FAKE, 0, 64, FAKE, FAKE, need,
+             ctypes.byref(d), None) == 0
+
+
 def test_check_calls_validate_on_host(cuda_lib):
     assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, None, None) == 1
     assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, FAKE, None) == 3  # bitmap small
