@@ -37,6 +37,7 @@ METRIC = "extend+decode attention tokens/s; HBM GB/s and TC util vs GB300 peak"
 WORKLOAD_NAMES = {1: "tiny", 2: "decode_llama7b", 3: "shared_prompt_extend",
                   4: "tree_of_thought_decode", 5: "chunked_prefill_mix"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+FP8_SCALE = 1.0 / 64  # per-tensor K and V scale of an e4m3 pool: N(0,1) rows stay inside +-448
 
 
 # ----------------------------------------------------------------- helpers
@@ -163,12 +164,28 @@ def barrier():
 class Step:
     """Device buffers of one workload and the launches of one step."""
 
-    def __init__(self, w: W.Workload, device, cascade: str = "off"):
+    def __init__(self, w: W.Workload, device, cascade: str = "off", kv: str = "bf16"):
         import torch
         from radixattention_prefix_shared_gb300 import binding as B
         self.B, self.torch, self.w, self.dev = B, torch, w, device
         t = W.to_device(w, device)
         self.t = t
+        self.fp8 = kv == "fp8"
+        if self.fp8:
+            if w.extend is not None:
+                raise SystemExit("--kv fp8: extend over an e4m3 pool is not built; use a decode-only workload")
+            # the cached rows pass through the quantising store once (setup);
+            # one scale per tensor, as a checkpoint provides
+            self.k_scale = self.v_scale = FP8_SCALE
+            pk8 = torch.zeros(t["pool_k"].shape, dtype=torch.uint8, device=device)
+            pv8 = torch.zeros_like(pk8)
+            live = torch.from_numpy(w.live_slots.astype(np.int64)).to(device)
+            for a in range(0, live.numel(), 1 << 16):
+                idx = live[a: a + (1 << 16)]
+                B.sgl_store_kv_fp8(t["pool_k"][idx].contiguous(), t["pool_v"][idx].contiguous(),
+                                   idx.to(torch.int32), pk8, pv8, self.k_scale, self.v_scale)
+            torch.cuda.synchronize()
+            t["pool_k"], t["pool_v"] = pk8, pv8
         d = w.dims
         self.Hq, self.Hkv, self.D = d.num_q_heads, d.num_kv_heads, d.head_dim
         # one store_kv over every new token: the extend and first-decode k/v
@@ -197,7 +214,9 @@ class Step:
         # off its rows once here (the host side of a serving loop keeps them
         # in its radix tree); "auto" uses them when the batch shares prefixes
         self.groups = []
-        if cascade != "off" and w.decode:
+        if cascade == "on" and self.fp8:
+            raise SystemExit("--kv fp8: cascade decode over an e4m3 pool is not built")
+        if cascade != "off" and w.decode and not self.fp8:
             self.groups = [W.tree_groups(w, s) for s in range(len(w.decode))]
             if cascade == "auto" and not any(g.n_groups for g in self.groups):
                 self.groups = []
@@ -224,7 +243,7 @@ class Step:
         launches = 0
         if ev is not None:
             ev[0].record()
-        B.sgl_store_kv(self.k_all, self.v_all, self.s_all, t["pool_k"], t["pool_v"])
+        self.store(self.k_all, self.v_all, self.s_all)
         launches += 1
         if ev is not None:
             ev[1].record()
@@ -239,7 +258,7 @@ class Step:
             ev[2].record()
         for s, (b, tb) in enumerate(zip(w.decode, t["decode"])):
             if s > 0:
-                B.sgl_store_kv(tb["k_new"], tb["v_new"], tb["slots"], t["pool_k"], t["pool_v"])
+                self.store(tb["k_new"], tb["v_new"], tb["slots"])
                 launches += 1
             if self.cascade:
                 g = self.groups[s]
@@ -249,6 +268,12 @@ class Step:
                                                max_group_members=max(g.max_members, 1),
                                                max_depth=max(g.max_depth, 1), workspace=self.ws_dec[s])
                 launches += 4 if g.n_groups else 3   # plan, groups, split, combine
+            elif self.fp8:
+                B.sgl_decode_attention_fp8(tb["q"], t["pool_k"], t["pool_v"], self.k_scale, self.v_scale,
+                                           t["req_to_token"], tb["req_pool_idx"], tb["seq_lens"],
+                                           self.out_dec[s], max_seq_len=int(b.seq_lens.max()),
+                                           workspace=self.ws_dec[s])
+                launches += 3                        # plan, split, combine
             else:
                 B.sgl_decode_attention(tb["q"], t["pool_k"], t["pool_v"], t["req_to_token"],
                                        tb["req_pool_idx"], tb["seq_lens"], self.out_dec[s],
@@ -257,6 +282,13 @@ class Step:
         if ev is not None:
             ev[3].record()
         self.launches = launches
+
+    def store(self, k, v, slots):
+        t = self.t
+        if self.fp8:
+            self.B.sgl_store_kv_fp8(k, v, slots, t["pool_k"], t["pool_v"], self.k_scale, self.v_scale)
+        else:
+            self.B.sgl_store_kv(k, v, slots, t["pool_k"], t["pool_v"])
 
     def twin(self):
         """A second set of per-step input/output buffers over the same pools
@@ -314,7 +346,7 @@ def small_kwargs(args):
     return SMALL.get(args.config, {}) if getattr(args, "small", False) else {}
 
 
-def work_of(w: W.Workload, groups=()):
+def work_of(w: W.Workload, groups=(), kv_elem_bytes=2):
     d = w.dims
     flops = 0
     ext_bytes = 0
@@ -322,13 +354,14 @@ def work_of(w: W.Workload, groups=()):
         e = w.extend
         flops = WM.extend_flops(e.prefix_lens, e.extend_lens, d.num_q_heads, d.head_dim)
         ext_bytes = WM.extend_bytes(e.prefix_lens, e.extend_lens, d.num_q_heads, d.num_kv_heads, d.head_dim)
-    dec_bytes = sum(WM.decode_bytes(b.seq_lens, d.num_q_heads, d.num_kv_heads, d.head_dim) for b in w.decode)
+    dec_bytes = sum(WM.decode_bytes(b.seq_lens, d.num_q_heads, d.num_kv_heads, d.head_dim, kv_elem_bytes)
+                    for b in w.decode)
     # with cascade groups each shared group's keys are read once per step
     dec_unique = sum(WM.cascade_decode_bytes(g.group_len, g.shared_lens(b.q.shape[0]), b.seq_lens,
                                              d.num_q_heads, d.num_kv_heads, d.head_dim)
                      for g, b in zip(groups, w.decode)) if groups else dec_bytes
     n_new = (w.extend.total_extend if w.extend is not None else 0) + sum(b.q.shape[0] for b in w.decode)
-    st_bytes = WM.store_kv_bytes(n_new, d.num_kv_heads, d.head_dim)
+    st_bytes = WM.store_kv_bytes(n_new, d.num_kv_heads, d.head_dim, kv_elem_bytes)
     return dict(extend_flops=flops, extend_bytes=ext_bytes, decode_bytes=dec_bytes,
                 decode_read_once_bytes=dec_unique, store_bytes=st_bytes)
 
@@ -359,8 +392,8 @@ def gpu_arm(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.make(args.config, seed=1000 + args.config + 7919 * rank, **small_kwargs(args))
-    step = Step(w, dev, args.cascade)
-    work = work_of(w, step.groups)
+    step = Step(w, dev, args.cascade, args.kv)
+    work = work_of(w, step.groups, 1 if step.fp8 else 2)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
     stream = torch.cuda.current_stream()
 
@@ -495,7 +528,7 @@ def gpu_arm(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if step.fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": wl + ("(small)" if args.small else ""), "num_q_heads": d.num_q_heads, "num_kv_heads": d.num_kv_heads,
                    "head_dim": d.head_dim, "pool_slots": d.pool_size,
@@ -504,6 +537,7 @@ def gpu_arm(args):
                    "query_tokens_per_step": int(step.tokens), "parallelism": f"replicas{world}",
                    "decode_path": ("cascade" if step.cascade else "plain") if w.decode else None,
                    "launch": "cuda_graph" if graph is not None else "eager",
+                   "kv_cache_dtype": "fp8_e4m3" if step.fp8 else "bf16",
                    "l2": "flushed between steps (256 MiB write)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_bytes),
                 "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e_ms, 4),
@@ -626,6 +660,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=5, choices=sorted(WORKLOAD_NAMES))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="KV pool element type (fp8: e4m3 codes with per-tensor scales; decode-only workloads)")
     ap.add_argument("--graph", choices=["on", "off"], default="on",
                     help="time the step replayed as one CUDA graph (per-kernel times stay eager)")
     ap.add_argument("--cascade", choices=["auto", "on", "off"], default="auto",

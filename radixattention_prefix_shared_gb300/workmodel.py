@@ -19,12 +19,14 @@ def kv_bytes_per_token(num_kv_heads: int, head_dim: int, layers: int = 1, elem_b
     return int(num_kv_heads) * 2 * int(head_dim) * int(layers) * int(elem_bytes)
 
 
-def decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
-    """K+V rows of every key, the int32 slot index of every key, q in, out."""
+def decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 kv_elem_bytes: int = 2) -> int:
+    """K+V rows of every key (2-byte bf16 or 1-byte e4m3 values), the int32
+    slot index of every key, q in, out (bf16)."""
     seq = np.asarray(seq_lens, dtype=np.int64)
     n_keys = int(seq.sum())
     B = int(seq.size)
-    return (n_keys * kv_bytes_per_token(num_kv_heads, head_dim)
+    return (n_keys * kv_bytes_per_token(num_kv_heads, head_dim, elem_bytes=kv_elem_bytes)
             + 4 * n_keys + 2 * 2 * B * num_q_heads * head_dim)
 
 
@@ -71,6 +73,8 @@ def extend_bytes(prefix_lens, extend_lens, num_q_heads, num_kv_heads, head_dim) 
     return p * kv + 4 * p + T * kv + 2 * 2 * T * num_q_heads * head_dim
 
 
-def store_kv_bytes(n: int, num_kv_heads: int, head_dim: int) -> int:
-    """Read n new K and V rows, write them to their slots, read n slot ids."""
-    return 2 * n * kv_bytes_per_token(num_kv_heads, head_dim) + 4 * int(n)
+def store_kv_bytes(n: int, num_kv_heads: int, head_dim: int, kv_elem_bytes: int = 2) -> int:
+    """Read n new bf16 K and V rows, write them to their slots (bf16, or e4m3
+    codes), read n slot ids."""
+    return (n * kv_bytes_per_token(num_kv_heads, head_dim)
+            + n * kv_bytes_per_token(num_kv_heads, head_dim, elem_bytes=kv_elem_bytes) + 4 * int(n))
