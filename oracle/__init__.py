@@ -27,6 +27,10 @@ What it computes, and where the pages fix it:
     quantised from the float32 quotient x / scale, decode over the
     dequantised rows -- "Inside SGLang", Step 6 (Decide how much memory
     becomes KV cache: --kv-cache-dtype fp8_e4m3, scales from the checkpoint).
+  * radix tree (``oracle.radix``): token runs with their KV slots, match
+    with node splitting, insert, lock counts on the path to the root,
+    leaf-first LRU eviction -- "Inside SGLang", Step 4 and the "SGLang"
+    notes (RadixAttention, Eviction).
 All arithmetic is float64.  Every function is pinned by ``tests/test_oracle.py``
 against closed forms, a library routine (full causal attention recomputed from
 scratch), invariants and brute force; see that file for the list.
@@ -44,3 +48,4 @@ from .attention import (  # noqa: F401
     cascade_decode_attention,
 )
 from . import fp8  # noqa: F401
+from . import radix  # noqa: F401
