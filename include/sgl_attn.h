@@ -316,6 +316,62 @@ sgl_status sgl_check_cascade_groups(const int32_t* req_to_token, int32_t rtt_row
                                     int32_t max_group_members, int32_t max_depth, void* scratch,
                                     size_t scratch_bytes, int32_t* d_error, sgl_stream_t stream);
 
+/*
+ * Radix tree of cached token runs (host only; no device memory, no CUDA call).
+ *
+ * The structure that lays out req_to_token rows ("Inside SGLang", Step 4:
+ * Grow a prefix tree, then run out of room; "SGLang" notes, RadixAttention
+ * and Eviction): each node holds a run of token ids, the KV-pool slots of
+ * those tokens, children keyed by first token, and a lock count.
+ *   match_prefix -- walk down while tokens agree; if the match ends inside a
+ *                   node, split it there.  Returns the matched length m
+ *                   (-1 on a bad argument), writes the path's slots
+ *                   (min(m, cap) of them) and the last matched node's handle
+ *                   (the root when m = 0).  Every node passed gets a new
+ *                   access time.
+ *   insert       -- the same walk, then the unmatched rest becomes a leaf
+ *                   holding slots[m..n).  Returns m: slots[0..m) duplicate
+ *                   cached tokens and are the caller's to free.
+ *   inc/dec_lock_ref -- lock (unlock) a node and its path to the root; a
+ *                   running request locks the last node it matched.  A split
+ *                   copies the lock count to the new prefix node.  Stale
+ *                   handles (of evicted nodes) and unbalanced decrements
+ *                   return SGL_ERR_INVALID_ARG and change nothing.
+ *   evict        -- free unlocked leaves, least recently used first (access
+ *                   times from a logical clock; ties by creation order), a
+ *                   parent that becomes a leaf joining the candidates, until
+ *                   at least num_tokens tokens are freed, nothing evictable is
+ *                   left, or the next leaf would not fit in `cap`.  Writes the
+ *                   freed slots (each leaf's in token order) and returns their
+ *                   count.
+ *   groups       -- the shared-prefix groups of a decode batch whose request
+ *                   r matched node nodes[r]: every non-root node on two or
+ *                   more requests' paths (start = position of its first token,
+ *                   len = its run, depth = its rank on the paths, members in
+ *                   ascending order), listed by (depth, start, first member) --
+ *                   the input of sgl_cascade_decode_attention.  Returns the
+ *                   group count and sets *n_members_out; the arrays
+ *                   (member_off holds n_groups + 1 entries) are written only
+ *                   when the counts fit cap_groups and cap_members.
+ * A tree is not thread-safe: one thread (the scheduler) owns it.
+ */
+typedef struct sgl_radix_tree sgl_radix_tree;
+sgl_radix_tree* sgl_radix_create(void);
+void sgl_radix_destroy(sgl_radix_tree* tree);
+int32_t sgl_radix_match_prefix(sgl_radix_tree* tree, const int32_t* tokens, int32_t n,
+                               int32_t* slots_out, int32_t cap, int64_t* node_out);
+int32_t sgl_radix_insert(sgl_radix_tree* tree, const int32_t* tokens, const int32_t* slots,
+                         int32_t n);
+sgl_status sgl_radix_inc_lock_ref(sgl_radix_tree* tree, int64_t node);
+sgl_status sgl_radix_dec_lock_ref(sgl_radix_tree* tree, int64_t node);
+int32_t sgl_radix_evict(sgl_radix_tree* tree, int32_t num_tokens, int32_t* slots_out, int32_t cap);
+int64_t sgl_radix_evictable_tokens(const sgl_radix_tree* tree);
+int64_t sgl_radix_protected_tokens(const sgl_radix_tree* tree);
+int32_t sgl_radix_groups(const sgl_radix_tree* tree, const int64_t* nodes, int32_t batch,
+                         int32_t* group_start, int32_t* group_len, int32_t* group_depth,
+                         int32_t* member_off, int32_t* members, int32_t cap_groups,
+                         int32_t cap_members, int32_t* n_members_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -55,6 +55,16 @@ _SIGS = {
                                                     c_i32, c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims),
                                                     c_vp]),
     "sgl_cascade_decode_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, _P(sgl_attn_dims)]),
+    "sgl_radix_create": (c_vp, []),
+    "sgl_radix_destroy": (None, [c_vp]),
+    "sgl_radix_match_prefix": (c_i32, [c_vp, c_vp, c_i32, c_vp, c_i32, _P(c_i64)]),
+    "sgl_radix_insert": (c_i32, [c_vp, c_vp, c_vp, c_i32]),
+    "sgl_radix_inc_lock_ref": (ctypes.c_int, [c_vp, c_i64]),
+    "sgl_radix_dec_lock_ref": (ctypes.c_int, [c_vp, c_i64]),
+    "sgl_radix_evict": (c_i32, [c_vp, c_i32, c_vp, c_i32]),
+    "sgl_radix_evictable_tokens": (c_i64, [c_vp]),
+    "sgl_radix_protected_tokens": (c_i64, [c_vp]),
+    "sgl_radix_groups": (c_i32, [c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, _P(c_i32)]),
     "sgl_store_kv_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_f32, c_f32,
                                         _P(sgl_attn_dims), c_vp]),
     "sgl_decode_attention_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_f32, c_f32, c_vp, c_i32, c_i32, c_vp,
@@ -278,3 +288,85 @@ def sgl_decode_attention_fp8(q, pool_k, pool_v, k_scale, v_scale, req_to_token, 
         int(max_seq_len), _ptr(out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
         ctypes.byref(d), _stream(stream)))
     return out
+
+
+# ----------------------------------------------------------------- radix tree
+
+class RadixTree:
+    """The library's radix tree of cached token runs (host side, C++).
+
+    Token ids and slots are int sequences; node handles are ints."""
+
+    def __init__(self):
+        self._t = lib().sgl_radix_create()
+        if not self._t:
+            raise MemoryError("sgl_radix_create failed")
+
+    def __del__(self):
+        if getattr(self, "_t", None):
+            lib().sgl_radix_destroy(self._t)
+            self._t = None
+
+    @staticmethod
+    def _arr(xs):
+        import numpy as np
+        return np.ascontiguousarray(np.asarray(xs, dtype=np.int32))
+
+    def match_prefix(self, tokens):
+        """(matched length, slots along the path, last node handle)."""
+        toks = self._arr(tokens)
+        out = self._arr([0] * max(1, toks.size))
+        node = c_i64(0)
+        m = lib().sgl_radix_match_prefix(self._t, toks.ctypes.data, int(toks.size), out.ctypes.data,
+                                         int(out.size), ctypes.byref(node))
+        if m < 0:
+            raise SglError("sgl_radix_match_prefix", 1)
+        return int(m), out[:m].tolist(), int(node.value)
+
+    def insert(self, tokens, slots):
+        toks, sl = self._arr(tokens), self._arr(slots)
+        if toks.size != sl.size:
+            raise ValueError("one slot per token")
+        m = lib().sgl_radix_insert(self._t, toks.ctypes.data, sl.ctypes.data, int(toks.size))
+        if m < 0:
+            raise SglError("sgl_radix_insert", 1)
+        return int(m)
+
+    def inc_lock_ref(self, node):
+        _check("sgl_radix_inc_lock_ref", lib().sgl_radix_inc_lock_ref(self._t, int(node)))
+
+    def dec_lock_ref(self, node):
+        _check("sgl_radix_dec_lock_ref", lib().sgl_radix_dec_lock_ref(self._t, int(node)))
+
+    def evict(self, num_tokens):
+        cap = int(self.evictable_tokens) + 1
+        out = self._arr([0] * cap)
+        n = lib().sgl_radix_evict(self._t, int(num_tokens), out.ctypes.data, cap)
+        if n < 0:
+            raise SglError("sgl_radix_evict", 1)
+        return out[:n].tolist()
+
+    @property
+    def evictable_tokens(self):
+        return int(lib().sgl_radix_evictable_tokens(self._t))
+
+    @property
+    def protected_tokens(self):
+        return int(lib().sgl_radix_protected_tokens(self._t))
+
+    def groups(self, nodes):
+        """Shared-prefix groups of a batch: (start, len, depth, member_off, members) int32 arrays."""
+        import numpy as np
+        hs = np.ascontiguousarray(np.asarray(nodes, dtype=np.int64))
+        nm = c_i32(0)
+        ng = lib().sgl_radix_groups(self._t, hs.ctypes.data, int(hs.size), None, None, None, None, None,
+                                    0, 0, ctypes.byref(nm))
+        if ng < 0:
+            raise SglError("sgl_radix_groups", 1)
+        start, length, depth = (np.zeros(ng, np.int32) for _ in range(3))
+        off, mem = np.zeros(ng + 1, np.int32), np.zeros(max(1, nm.value), np.int32)
+        ng2 = lib().sgl_radix_groups(self._t, hs.ctypes.data, int(hs.size), start.ctypes.data,
+                                     length.ctypes.data, depth.ctypes.data, off.ctypes.data, mem.ctypes.data,
+                                     ng, int(mem.size), ctypes.byref(nm))
+        assert ng2 == ng
+        return start, length, depth, off, mem[: nm.value]
