@@ -14,13 +14,16 @@
 //                 per-KV-head counter; y: KV head) runs
 //                 each item: the slot indices go to shared memory, K and V
 //                 rows of the KV head are gathered by 16-byte cp.async into a
-//                 kStages-deep ring of tiles (32 bf16 or 64 e4m3 keys), and the query heads of
-//                 the group share every loaded row.  LPT (8 or 16) lanes own one
-//                 key, each lane a slice of the head dim; every lane group keeps its own
-//                 fp32 online-softmax state (max, sum, weighted V sum) with
-//                 warp-shuffle reductions, and the groups and warps are merged
-//                 at the end of the item.  Requests with one split write the
-//                 output directly; others write their partial state;
+//                 kStages-deep ring of tiles (32 bf16 or 64 e4m3 keys), and
+//                 the query heads of the group share every loaded row.  Each
+//                 warp takes a quarter of a tile: with one or two query heads
+//                 per KV head on CUDA cores (LPT = 8 or 16 lanes own one key,
+//                 each lane a slice of the head dim, every lane group an fp32
+//                 online-softmax state), with four or more on tensor cores
+//                 (warp-level MMAs whose rows are the query heads).  The
+//                 warps' states are merged at the end of the item.  Requests
+//                 with one split write the output directly; others write
+//                 their partial state;
 //   3. combine -- one warp per (request, query head) merges the partial
 //                 states of multi-split requests (max-rescaled sums).
 // Cascade decode (shared prefixes read once per group) runs the same three
@@ -32,6 +35,8 @@
 // running max is only moved when a score exceeds it by more than 2^8, which
 // keeps every exponentiated weight <= 256 in fp32 and makes rescaling rare.
 #include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -252,28 +257,380 @@ SGL_DEV void load_row_chunk(const uint8_t* p, float* f) {
   }
 }
 
+// Warp-level tensor-core products for the MMA path (rows = the G query
+// heads of a KV head, padded to 16; rows 8-15 are always zero).
+SGL_DEV void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+SGL_DEV void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+SGL_DEV void mma_1688_bf16(float (&d)[4], uint32_t a0, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(b0));
+}
+// two e4m3 codes (low byte first) -> f16x2 bits
+SGL_DEV uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+SGL_DEV uint32_t pack_f16x2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 template <int D, int G, int LPT>
-constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
+__host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
+
+#ifndef SGL_DECODE_MMA
+#define SGL_DECODE_MMA 2
+#endif
+// Which (pool type, group size) take the tensor-core path: 0 none, 1 all, 2
+// (measured best) G >= 4, or G >= 2 on an e4m3 pool.  With one or two bf16
+// query heads per KV head the 16-row MMAs carry 14-15 empty rows and the
+// CUDA-core path is faster; from four heads on the MMAs remove most of the
+// per-key instructions (tree decode 23% faster at G = 4).
+template <typename KV, int G>
+__host__ __device__ constexpr bool use_mma() {
+  return SGL_DECODE_MMA == 1 || (SGL_DECODE_MMA == 2 && (G >= 4 || (sizeof(KV) == 1 && G >= 2)));
+}
+
+// Per-warp attention state of the CUDA-core path: LPT lanes own one key, each
+// lane a slice of the head dim; every lane group keeps an fp32 online-softmax
+// state (max, sum, weighted V sum) for each of the G query heads.
+template <int D, int G, int LPT, typename KV, int kTile>
+struct FmaState {
+  using L = Lane<D, LPT, KV>;
+  static constexpr int EL = L::kElems, CE = L::kChunkElems;
+  float qf[G][EL];
+  float m[G], l[G], acc[G][EL];
+  int grp, li, warp;
+
+  SGL_DEV void init(int lane, int w) {
+    grp = lane / LPT;
+    li = lane % LPT;
+    warp = w;
+  }
+  // this lane's slice of the G query heads, pre-scaled into log2 units
+  SGL_DEV void load_q(const __nv_bfloat16* qb, float scale_log2) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll
+        for (int u = 0; u < CE; u += 8) {
+          uint4 raw = *reinterpret_cast<const uint4*>(qb + h * D + L::elem(c, li) + u);
+          bf16x8_to_f32(raw, &qf[h][c * CE + u]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qf[h][c * CE + u + e] *= scale_log2;
+        }
+  }
+  SGL_DEV void reset() {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EL; ++e) acc[h][e] = 0.f;
+    }
+  }
+  // the stage's keys key0 .. key0 + kTile (those < n are valid)
+  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float) {
+#pragma unroll
+    for (int sub = 0; sub < kTile / (L::kGroups * kWarps); ++sub) {
+      const int tok = warp * (kTile / kWarps) + sub * L::kGroups + grp;
+      const bool valid = key0 + tok < n;
+      float kf[EL];
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        load_row_chunk<KV, CE>(ks + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &kf[c * CE]);
+      // q.k and p.v on the packed fp32 pipe (two lanes of FMA per instruction)
+      float s[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < EL; e += 2)
+          a = ffma2(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+        s[h] = a.x + a.y;
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int o = 1; o < LPT; o <<= 1) s[h] += __shfl_xor_sync(0xffffffffu, s[h], o);
+        if (!valid) s[h] = -INFINITY;
+      }
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < G; ++h) need |= s[h] > m[h] + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          if (s[h] > m[h] + kRescaleThreshold) {
+            const float a = ex2(m[h] - s[h]);
+            m[h] = s[h];
+            l[h] *= a;
+#pragma unroll
+            for (int e = 0; e < EL; ++e) acc[h][e] *= a;
+          }
+        }
+      }
+      float vf[EL];
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        load_row_chunk<KV, CE>(vs + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &vf[c * CE]);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pw = valid ? ex2(s[h] - m[h]) : 0.f;
+        l[h] += pw;
+#pragma unroll
+        for (int e = 0; e < EL; e += 2) {
+          const float2 a = ffma2(make_float2(pw, pw), make_float2(vf[e], vf[e + 1]),
+                                 make_float2(acc[h][e], acc[h][e + 1]));
+          acc[h][e] = a.x;
+          acc[h][e + 1] = a.y;
+        }
+      }
+    }
+  }
+  // merge the warp's lane groups and write its state to the CTA scratch
+  SGL_DEV void publish(float* red_acc, float* red_m, float* red_l) {
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+        const float mn = fmaxf(m[h], mo);
+        const float fa = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
+        const float fb = mo == -INFINITY ? 0.f : ex2(mo - mn);
+        l[h] = l[h] * fa + lo * fb;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+          const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+          acc[h][e] = acc[h][e] * fa + ao * fb;
+        }
+        m[h] = mn;
+      }
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll
+          for (int e = 0; e < CE; ++e)
+            red_acc[(warp * G + h) * D + L::elem(c, li) + e] = acc[h][c * CE + e];
+        if (li == 0) {
+          red_m[warp * G + h] = m[h];
+          red_l[warp * G + h] = l[h];
+        }
+      }
+    }
+  }
+};
+
+// Per-warp attention state of the tensor-core path: the G query heads are the
+// rows of warp-level MMAs (m16n8k16 / m16n8k8, rows G..15 zero), lane (g, t)
+// = (lane / 4, lane % 4).  q.k contracts over the head dim in an order both
+// operands share (lane t holds dims [t*D/4, (t+1)*D/4) of its row, four per
+// k-step), so each lane's K row slice is one run of 16-byte loads; p.v
+// permutes the output columns so that lane g's V loads are contiguous (n-col
+// g of 8-column block j of 32-column block sb is dim 32*sb + 4*g + j; lane
+// (g, t) ends up holding dims 32*sb + 8*t .. +7 of head g).  bf16 pools use
+// bf16 operands; e4m3 pools convert codes to f16 operands two at a time.
+// Accumulation and the online softmax stay fp32; P is rounded to the operand
+// type before the p.v product.
+template <int D, int G, typename KV, int kTile>
+struct MmaState {
+  static constexpr int kBytes = (int)sizeof(KV);
+  static constexpr int kRowBytes = D * kBytes;
+  static constexpr int KS = D / 16;          // k-steps of q.k
+  static constexpr int SB = D / 32;          // 32-column blocks of p.v
+  static constexpr int KW = kTile / kWarps;  // keys of a warp per stage: 8 bf16, 16 e4m3
+  static constexpr int DL = D / 4;           // head-dim values of one lane in q.k
+  static_assert(G <= 8, "rows 8..15 of the MMA are padding");
+  static_assert(KW == (kBytes == 2 ? 8 : 16), "stage shape");
+  uint32_t qa[KS][2];
+  float o[SB][4][4];
+  float m, l;
+  int g, t, warp;
+
+  SGL_DEV void init(int lane, int w) {
+    g = lane >> 2;
+    t = lane & 3;
+    warp = w;
+  }
+  SGL_DEV void load_q(const __nv_bfloat16* qb, float) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
+    if (g < G) {
+      const uint4* src = reinterpret_cast<const uint4*>(qb + g * D + DL * t);
+#pragma unroll
+      for (int v = 0; v < DL / 8; ++v) {
+        const uint4 w = src[v];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t x = ws[i];
+          if constexpr (kBytes == 1)
+            x = pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+          qa[(4 * v + i) / 2][(4 * v + i) % 2] = x;
+        }
+      }
+    }
+  }
+  SGL_DEV void reset() {
+    m = -INFINITY;
+    l = 0.f;
+#pragma unroll
+    for (int b = 0; b < SB; ++b)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[b][j][c] = 0.f;
+  }
+  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2) {
+    // ---- S = q.k for this warp's KW keys, 8 at a time
+    float sv[KW / 8][2];
+#pragma unroll
+    for (int nb = 0; nb < KW / 8; ++nb) {
+      const uint8_t* row = ks + (warp * KW + nb * 8 + g) * kRowBytes + DL * t * kBytes;
+      float d4[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (kBytes == 2) {
+#pragma unroll
+        for (int v = 0; v < DL / 8; ++v) {  // 8 bf16 = two k-steps
+          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
+          mma_16816_bf16(d4, qa[2 * v][0], qa[2 * v][1], w.x, w.y);
+          mma_16816_bf16(d4, qa[2 * v + 1][0], qa[2 * v + 1][1], w.z, w.w);
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < DL / 16; ++v) {  // 16 codes = four k-steps
+          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mma_16816_f16(d4, qa[4 * v + i][0], qa[4 * v + i][1], e4m3x2_to_f16x2(ws[i]),
+                          e4m3x2_to_f16x2(ws[i] >> 16));
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        sv[nb][c] = key0 + warp * KW + nb * 8 + 2 * t + c < n ? d4[c] * scale_log2 : -INFINITY;
+    }
+    // ---- online softmax of row g (the 4 lanes of the row agree on m)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < KW / 8; ++nb) mx = fmax3(mx, sv[nb][0], sv[nb][1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (mx > m + kRescaleThreshold) {
+      const float a = m == -INFINITY ? 0.f : ex2(m - mx);
+      m = mx;
+      l *= a;
+#pragma unroll
+      for (int b = 0; b < SB; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          o[b][j][0] *= a;
+          o[b][j][1] *= a;
+        }
+    }
+    float pv[KW / 8][2];
+#pragma unroll
+    for (int nb = 0; nb < KW / 8; ++nb)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        pv[nb][c] = sv[nb][c] == -INFINITY ? 0.f : ex2(sv[nb][c] - m);
+        l += pv[nb][c];
+      }
+    // ---- O += P V
+    const uint8_t* r0 = vs + (warp * KW + 2 * t) * kRowBytes;  // key 2t of this warp's keys
+    if constexpr (kBytes == 2) {
+      const uint32_t a0 = pack_bf16x2(pv[0][0], pv[0][1]);
+#pragma unroll
+      for (int b = 0; b < SB; ++b) {
+        const uint2 x = *reinterpret_cast<const uint2*>(r0 + 2 * (32 * b + 4 * g));
+        const uint2 y = *reinterpret_cast<const uint2*>(r0 + kRowBytes + 2 * (32 * b + 4 * g));
+        mma_1688_bf16(o[b][0], a0, __byte_perm(x.x, y.x, 0x5410));
+        mma_1688_bf16(o[b][1], a0, __byte_perm(x.x, y.x, 0x7632));
+        mma_1688_bf16(o[b][2], a0, __byte_perm(x.y, y.y, 0x5410));
+        mma_1688_bf16(o[b][3], a0, __byte_perm(x.y, y.y, 0x7632));
+      }
+    } else {
+      const uint32_t a0 = pack_f16x2(pv[0][0], pv[0][1]), a2 = pack_f16x2(pv[1][0], pv[1][1]);
+#pragma unroll
+      for (int b = 0; b < SB; ++b) {
+        const int col = 32 * b + 4 * g;
+        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(r0 + col);
+        const uint32_t x1 = *reinterpret_cast<const uint32_t*>(r0 + kRowBytes + col);
+        const uint32_t y0 = *reinterpret_cast<const uint32_t*>(r0 + 8 * kRowBytes + col);
+        const uint32_t y1 = *reinterpret_cast<const uint32_t*>(r0 + 9 * kRowBytes + col);
+        const uint32_t xa = __byte_perm(x0, x1, 0x5140), xb = __byte_perm(x0, x1, 0x7362);
+        const uint32_t ya = __byte_perm(y0, y1, 0x5140), yb = __byte_perm(y0, y1, 0x7362);
+        mma_16816_f16(o[b][0], a0, a2, e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(ya));
+        mma_16816_f16(o[b][1], a0, a2, e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(ya >> 16));
+        mma_16816_f16(o[b][2], a0, a2, e4m3x2_to_f16x2(xb), e4m3x2_to_f16x2(yb));
+        mma_16816_f16(o[b][3], a0, a2, e4m3x2_to_f16x2(xb >> 16), e4m3x2_to_f16x2(yb >> 16));
+      }
+    }
+  }
+  SGL_DEV void publish(float* red_acc, float* red_m, float* red_l) {
+    float ls = l;
+    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    if (g < G) {
+      float* dst = red_acc + (warp * G + g) * D + 8 * t;
+#pragma unroll
+      for (int b = 0; b < SB; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dst[32 * b + j] = o[b][j][0];
+          dst[32 * b + 4 + j] = o[b][j][1];
+        }
+      if (t == 0) {
+        red_m[warp * G + g] = m;
+        red_l[warp * G + g] = ls;
+      }
+    }
+  }
+};
 
 template <int D, int G, int LPT, typename KV>
-__global__ void __launch_bounds__(kThreads, (min_blocks<D, G, LPT>()))
+__host__ __device__ constexpr int split_min_blocks() { return use_mma<KV, G>() ? 3 : min_blocks<D, G, LPT>(); }
+
+template <int D, int G, int LPT, typename KV>
+__global__ void __launch_bounds__(kThreads, (split_min_blocks<D, G, LPT, KV>()))
 decode_split_kernel(Params p) {
   using L = Lane<D, LPT, KV>;
-  constexpr int EL = L::kElems;
-  constexpr int CE = L::kChunkElems;
   // a stage holds the same bytes for either pool type (64 e4m3 keys or 32 bf16)
   constexpr int kTile = SGL_DECODE_TILE * 2 / L::kBytes;  // keys per pipeline stage
   constexpr int kTileBytes = kTile * L::kRowBytes;         // one K or V tile
   constexpr int kStageBytes = 2 * kTileBytes;              // K then V
+  using State = std::conditional_t<use_mma<KV, G>(), MmaState<D, G, KV, kTile>,
+                                   FmaState<D, G, LPT, KV, kTile>>;
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t* s_slots = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
   float* s_red = reinterpret_cast<float*>(smem);           // reuses the ring after an item
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grp = lane / LPT, li = lane % LPT;
   const int kvh = blockIdx.y;
   const int32_t n_items = *p.ws.n_items;
   const uint32_t ring = smem_u32(smem);
+  State st;
+  st.init(lane, warp);
   // items are taken dynamically from the KV head's counter; the next index
   // is fetched while the current item runs
   __shared__ int32_t s_item[2];
@@ -296,30 +653,14 @@ decode_split_kernel(Params p) {
     const int32_t n = base + (it.y < rem ? 1 : 0);
     const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride + t0;
     for (int i = tid; i < n; i += kThreads) s_slots[i] = rtt[i];
-
-    // this lane's slice of the G query heads, pre-scaled into log2 units
-    float qf[G][EL];
-    {
-      const __nv_bfloat16* qb = p.q + ((int64_t)r * p.Hq + (int64_t)kvh * G) * D;
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-#pragma unroll
-          for (int u = 0; u < CE; u += 8) {
-            uint4 raw = *reinterpret_cast<const uint4*>(qb + h * D + L::elem(c, li) + u);
-            bf16x8_to_f32(raw, &qf[h][c * CE + u]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qf[h][c * CE + u + e] *= p.scale_log2;
-          }
-    }
+    st.load_q(p.q + ((int64_t)r * p.Hq + (int64_t)kvh * G) * D, p.scale_log2);
     __syncthreads();  // slots visible; previous item's reduction scratch free
 
     const int n_tiles = (n + kTile - 1) / kTile;
     const uint8_t* kbase = p.pool_k + (int64_t)kvh * L::kRowBytes;
     const uint8_t* vbase = p.pool_v + (int64_t)kvh * L::kRowBytes;
     auto issue = [&](int tile, int stage) {
-      const uint32_t st = ring + stage * kStageBytes;
+      const uint32_t st_a = ring + stage * kStageBytes;
       constexpr int kRowsPerPass = kThreads / L::kRowVecs;
       const int vec = tid % L::kRowVecs;
 #pragma unroll
@@ -328,7 +669,7 @@ decode_split_kernel(Params p) {
         const int32_t j = tile * kTile + tok;
         const bool ok = j < n;
         const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv : 0;
-        const uint32_t d = st + tok * L::kRowBytes + vec * 16;
+        const uint32_t d = st_a + tok * L::kRowBytes + vec * 16;
         cp_async_16(d, kbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
         cp_async_16(d + kTileBytes, vbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
       }
@@ -338,120 +679,23 @@ decode_split_kernel(Params p) {
       if (s < n_tiles) issue(s, s);
       cp_async_commit();
     }
-
-    float m[G], l[G], acc[G][EL];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EL; ++e) acc[h][e] = 0.f;
-    }
-
+    st.reset();
     for (int k = 0; k < n_tiles; ++k) {
       cp_async_wait<kStages - 2>();
       __syncthreads();
       if (k + kStages - 1 < n_tiles) issue(k + kStages - 1, (k + kStages - 1) % kStages);
       cp_async_commit();
       const uint8_t* ks = smem + (k % kStages) * kStageBytes;
-      const uint8_t* vs = ks + kTileBytes;
-#pragma unroll
-      for (int sub = 0; sub < kTile / (L::kGroups * kWarps); ++sub) {
-        const int tok = warp * (kTile / kWarps) + sub * L::kGroups + grp;
-        const bool valid = k * kTile + tok < n;
-        float kf[EL];
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          load_row_chunk<KV, CE>(ks + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &kf[c * CE]);
-        // q.k and p.v on the packed fp32 pipe (two lanes of FMA per instruction)
-        float s[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < EL; e += 2)
-            a = ffma2(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), a);
-          s[h] = a.x + a.y;
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-#pragma unroll
-          for (int o = 1; o < LPT; o <<= 1) s[h] += __shfl_xor_sync(0xffffffffu, s[h], o);
-          if (!valid) s[h] = -INFINITY;
-        }
-        bool need = false;
-#pragma unroll
-        for (int h = 0; h < G; ++h) need |= s[h] > m[h] + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            if (s[h] > m[h] + kRescaleThreshold) {
-              const float a = ex2(m[h] - s[h]);
-              m[h] = s[h];
-              l[h] *= a;
-#pragma unroll
-              for (int e = 0; e < EL; ++e) acc[h][e] *= a;
-            }
-          }
-        }
-        float vf[EL];
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          load_row_chunk<KV, CE>(vs + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &vf[c * CE]);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pw = valid ? ex2(s[h] - m[h]) : 0.f;
-          l[h] += pw;
-#pragma unroll
-          for (int e = 0; e < EL; e += 2) {
-            const float2 a = ffma2(make_float2(pw, pw), make_float2(vf[e], vf[e + 1]),
-                                   make_float2(acc[h][e], acc[h][e + 1]));
-            acc[h][e] = a.x;
-            acc[h][e + 1] = a.y;
-          }
-        }
-      }
+      st.stage(ks, ks + kTileBytes, k * kTile, n, p.scale_log2);
     }
     cp_async_wait_all();
 
-    // merge the lane groups of the warp (lanes with the same li)
-#pragma unroll
-    for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
-        const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
-        const float mn = fmaxf(m[h], mo);
-        const float fa = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
-        const float fb = mo == -INFINITY ? 0.f : ex2(mo - mn);
-        l[h] = l[h] * fa + lo * fb;
-#pragma unroll
-        for (int e = 0; e < EL; ++e) {
-          const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
-          acc[h][e] = acc[h][e] * fa + ao * fb;
-        }
-        m[h] = mn;
-      }
-    }
     __syncthreads();  // every warp is done with the ring; reuse it for the reduction
     // s_red layout: [warp][G][D] acc, then [warp][G] m, then [warp][G] l
     float* red_acc = s_red;
     float* red_m = s_red + kWarps * G * D;
     float* red_l = red_m + kWarps * G;
-    if (grp == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-#pragma unroll
-          for (int e = 0; e < CE; ++e)
-            red_acc[(warp * G + h) * D + L::elem(c, li) + e] = acc[h][c * CE + e];
-        if (li == 0) {
-          red_m[warp * G + h] = m[h];
-          red_l[warp * G + h] = l[h];
-        }
-      }
-    }
+    st.publish(red_acc, red_m, red_l);
     __syncthreads();
     const bool single = ns == 1 && info.y == 0;
     for (int idx = tid; idx < G * D; idx += kThreads) {
