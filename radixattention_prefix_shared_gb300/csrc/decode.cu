@@ -8,13 +8,14 @@
 //
 // Schedule (split-KV):
 //   1. plan    -- one block lists the work items (request, split): a
-//                 request's keys are cut into ceil(seq_len / kChunk) runs of
+//                 request's keys are cut into ceil(seq_len / 1024) runs of
 //                 near-equal length;
 //   2. split   -- a persistent grid (x: two waves of CTAs taking items from a
 //                 per-KV-head counter; y: KV head) runs
 //                 each item: the slot indices go to shared memory, K and V
 //                 rows of the KV head are gathered by 16-byte cp.async into a
-//                 kStages-deep ring of tiles (32 bf16 or 64 e4m3 keys), and
+//                 ring of tiles (CUDA-core path: 6 stages of 16 bf16 / 32 e4m3
+//                 keys; tensor-core path: 4 stages of 32 / 64), and
 //                 the query heads of the group share every loaded row.  Each
 //                 warp takes a quarter of a tile: with one or two query heads
 //                 per KV head on CUDA cores (LPT = 8 or 16 lanes own one key,
@@ -46,7 +47,7 @@ namespace sgl {
 namespace {
 
 #ifndef SGL_DECODE_CHUNK
-#define SGL_DECODE_CHUNK 512
+#define SGL_DECODE_CHUNK 1024
 #endif
 #ifndef SGL_DECODE_TILE
 #define SGL_DECODE_TILE 32
@@ -55,6 +56,13 @@ namespace {
 #define SGL_DECODE_STAGES 4
 #endif
 constexpr int kChunk = SGL_DECODE_CHUNK;  // keys per work item
+// measured best for the CUDA-core path: a deeper ring of smaller tiles
+#ifndef SGL_DECODE_TILE_FMA
+#define SGL_DECODE_TILE_FMA 16
+#endif
+#ifndef SGL_DECODE_STAGES_FMA
+#define SGL_DECODE_STAGES_FMA 6
+#endif
 constexpr int kTileBf16 = SGL_DECODE_TILE;  // bf16 keys per pipeline stage (twice as many e4m3)
 constexpr int kStages = SGL_DECODE_STAGES;  // ring depth
 constexpr int kWarps = 4;
@@ -611,12 +619,26 @@ struct MmaState {
 template <int D, int G, int LPT, typename KV>
 __host__ __device__ constexpr int split_min_blocks() { return use_mma<KV, G>() ? 3 : min_blocks<D, G, LPT>(); }
 
+// Ring shape of the split kernel: the tensor-core path takes 32 bf16 keys per
+// stage (8 per warp), the CUDA-core path its own tile and depth.  A stage
+// holds the same bytes for either pool type (twice as many e4m3 keys).
+template <typename KV, int G>
+struct SplitRing {
+  static constexpr bool kMma = use_mma<KV, G>();
+  static constexpr int kTileB = kMma ? kTileBf16 : SGL_DECODE_TILE_FMA;  // bf16 keys per stage
+  static constexpr int kDepth = kMma ? kStages : SGL_DECODE_STAGES_FMA;
+  static constexpr int kTile = kTileB * 2 / (int)sizeof(KV);            // keys per stage
+  template <int D>
+  static constexpr size_t bytes() { return (size_t)kDepth * 2 * kTileB * D * 2; }
+};
+
 template <int D, int G, int LPT, typename KV>
 __global__ void __launch_bounds__(kThreads, (split_min_blocks<D, G, LPT, KV>()))
 decode_split_kernel(Params p) {
   using L = Lane<D, LPT, KV>;
-  // a stage holds the same bytes for either pool type (64 e4m3 keys or 32 bf16)
-  constexpr int kTile = SGL_DECODE_TILE * 2 / L::kBytes;  // keys per pipeline stage
+  using Ring = SplitRing<KV, G>;
+  constexpr int kTile = Ring::kTile;  // keys per pipeline stage
+  constexpr int kStages = Ring::kDepth;
   constexpr int kTileBytes = kTile * L::kRowBytes;         // one K or V tile
   constexpr int kStageBytes = 2 * kTileBytes;              // K then V
   using State = std::conditional_t<use_mma<KV, G>(), MmaState<D, G, KV, kTile>,
@@ -774,7 +796,7 @@ template <int D, int G, typename KV>
 sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const GroupArgs* ga,
                cudaStream_t stream) {
   constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
-  constexpr size_t kRing = (size_t)kStages * 2 * kTileBf16 * D * 2;  // same bytes for e4m3
+  constexpr size_t kRing = SplitRing<KV, G>::template bytes<D>();
   constexpr size_t smem = kRing + kChunk * sizeof(int32_t);
   static_assert(kWarps * G * (D + 2) * sizeof(float) <= kRing, "reduction scratch must fit in the ring");
   auto kern = decode_split_kernel<D, G, LPT, KV>;
