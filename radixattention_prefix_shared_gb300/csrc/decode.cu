@@ -308,10 +308,13 @@ __host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 
 // (measured best) G >= 4, or G >= 2 on an e4m3 pool.  With one or two bf16
 // query heads per KV head the 16-row MMAs carry 14-15 empty rows and the
 // CUDA-core path is faster; from four heads on the MMAs remove most of the
-// per-key instructions (tree decode 23% faster at G = 4).
+// per-key instructions (tree decode 23% faster at G = 4).  Group sizes the
+// CUDA-core path is not built for (3, 5, 6, 7, 16) always take it; above 8
+// heads the MMA rows 8..15 carry heads too.
 template <typename KV, int G>
 __host__ __device__ constexpr bool use_mma() {
-  return SGL_DECODE_MMA == 1 || (SGL_DECODE_MMA == 2 && (G >= 4 || (sizeof(KV) == 1 && G >= 2)));
+  return G == 3 || G > 4 || SGL_DECODE_MMA == 1 ||
+         (SGL_DECODE_MMA == 2 && (G >= 4 || (sizeof(KV) == 1 && G >= 2)));
 }
 
 // Per-warp attention state of the CUDA-core path: LPT lanes own one key, each
@@ -468,11 +471,13 @@ struct MmaState {
   static constexpr int SB = D / 32;          // 32-column blocks of p.v
   static constexpr int KW = kTile / kWarps;  // keys of a warp per stage: 8 bf16, 16 e4m3
   static constexpr int DL = D / 4;           // head-dim values of one lane in q.k
-  static_assert(G <= 8, "rows 8..15 of the MMA are padding");
+  static constexpr bool kTwoRows = G > 8;    // rows 8..15 carry heads too
+  static constexpr int NR = kTwoRows ? 2 : 1;  // rows of a lane: g (and g + 8)
+  static_assert(G <= 16, "at most 16 query heads per KV head");
   static_assert(KW == (kBytes == 2 ? 8 : 16), "stage shape");
-  uint32_t qa[KS][2];
-  float o[SB][4][4];
-  float m, l;
+  uint32_t qa[KS][2 * NR];  // per k-step: row g lo, row g hi (, row g+8 lo, row g+8 hi)
+  float o[SB][4][4];        // c0, c1: row g; c2, c3: row g + 8
+  float m[NR], l[NR];
   int g, t, warp;
 
   SGL_DEV void init(int lane, int w) {
@@ -482,26 +487,33 @@ struct MmaState {
   }
   SGL_DEV void load_q(const __nv_bfloat16* qb, float) {
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
-    if (g < G) {
-      const uint4* src = reinterpret_cast<const uint4*>(qb + g * D + DL * t);
+    for (int rr = 0; rr < NR; ++rr) {
+      const int row = g + 8 * rr;
 #pragma unroll
-      for (int v = 0; v < DL / 8; ++v) {
-        const uint4 w = src[v];
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      for (int ks = 0; ks < KS; ++ks) qa[ks][2 * rr] = qa[ks][2 * rr + 1] = 0u;
+      if (row < G) {
+        const uint4* src = reinterpret_cast<const uint4*>(qb + row * D + DL * t);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t x = ws[i];
-          if constexpr (kBytes == 1)
-            x = pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-          qa[(4 * v + i) / 2][(4 * v + i) % 2] = x;
+        for (int v = 0; v < DL / 8; ++v) {
+          const uint4 w = src[v];
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t x = ws[i];
+            if constexpr (kBytes == 1)
+              x = pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+            qa[(4 * v + i) / 2][2 * rr + (4 * v + i) % 2] = x;
+          }
         }
       }
     }
   }
   SGL_DEV void reset() {
-    m = -INFINITY;
-    l = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) {
+      m[rr] = -INFINITY;
+      l[rr] = 0.f;
+    }
 #pragma unroll
     for (int b = 0; b < SB; ++b)
 #pragma unroll
@@ -509,9 +521,29 @@ struct MmaState {
 #pragma unroll
         for (int c = 0; c < 4; ++c) o[b][j][c] = 0.f;
   }
+  SGL_DEV void qk(float (&d4)[4], int ks_, uint32_t b0, uint32_t b1) {
+    uint32_t a1 = 0u, a3 = 0u;  // rows g + 8
+    if constexpr (kTwoRows) {
+      a1 = qa[ks_][2];
+      a3 = qa[ks_][3];
+    }
+    if constexpr (kBytes == 2) {
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
+          : "r"(qa[ks_][0]), "r"(a1), "r"(qa[ks_][1]), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
+          : "r"(qa[ks_][0]), "r"(a1), "r"(qa[ks_][1]), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
   SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2) {
-    // ---- S = q.k for this warp's KW keys, 8 at a time
-    float sv[KW / 8][2];
+    // ---- S = q.k for this warp's KW keys, 8 at a time; sv[nb][row set][c]
+    float sv[KW / 8][NR][2];
 #pragma unroll
     for (int nb = 0; nb < KW / 8; ++nb) {
       const uint8_t* row = ks + (warp * KW + nb * 8 + g) * kRowBytes + DL * t * kBytes;
@@ -520,8 +552,8 @@ struct MmaState {
 #pragma unroll
         for (int v = 0; v < DL / 8; ++v) {  // 8 bf16 = two k-steps
           const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
-          mma_16816_bf16(d4, qa[2 * v][0], qa[2 * v][1], w.x, w.y);
-          mma_16816_bf16(d4, qa[2 * v + 1][0], qa[2 * v + 1][1], w.z, w.w);
+          qk(d4, 2 * v, w.x, w.y);
+          qk(d4, 2 * v + 1, w.z, w.w);
         }
       } else {
 #pragma unroll
@@ -530,55 +562,68 @@ struct MmaState {
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            mma_16816_f16(d4, qa[4 * v + i][0], qa[4 * v + i][1], e4m3x2_to_f16x2(ws[i]),
-                          e4m3x2_to_f16x2(ws[i] >> 16));
+            qk(d4, 4 * v + i, e4m3x2_to_f16x2(ws[i]), e4m3x2_to_f16x2(ws[i] >> 16));
         }
       }
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-        sv[nb][c] = key0 + warp * KW + nb * 8 + 2 * t + c < n ? d4[c] * scale_log2 : -INFINITY;
+      for (int rr = 0; rr < NR; ++rr)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          sv[nb][rr][c] =
+              key0 + warp * KW + nb * 8 + 2 * t + c < n ? d4[2 * rr + c] * scale_log2 : -INFINITY;
     }
-    // ---- online softmax of row g (the 4 lanes of the row agree on m)
-    float mx = -INFINITY;
+    // ---- online softmax of row g (and g + 8); the 4 lanes of a row agree on m
+    float pv[KW / 8][NR][2];
 #pragma unroll
-    for (int nb = 0; nb < KW / 8; ++nb) mx = fmax3(mx, sv[nb][0], sv[nb][1]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (mx > m + kRescaleThreshold) {
-      const float a = m == -INFINITY ? 0.f : ex2(m - mx);
-      m = mx;
-      l *= a;
+    for (int rr = 0; rr < NR; ++rr) {
+      float mx = -INFINITY;
 #pragma unroll
-      for (int b = 0; b < SB; ++b)
+      for (int nb = 0; nb < KW / 8; ++nb) mx = fmax3(mx, sv[nb][rr][0], sv[nb][rr][1]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (mx > m[rr] + kRescaleThreshold) {
+        const float a = m[rr] == -INFINITY ? 0.f : ex2(m[rr] - mx);
+        m[rr] = mx;
+        l[rr] *= a;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          o[b][j][0] *= a;
-          o[b][j][1] *= a;
+        for (int b = 0; b < SB; ++b)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            o[b][j][2 * rr] *= a;
+            o[b][j][2 * rr + 1] *= a;
+          }
+      }
+#pragma unroll
+      for (int nb = 0; nb < KW / 8; ++nb)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          pv[nb][rr][c] = sv[nb][rr][c] == -INFINITY ? 0.f : ex2(sv[nb][rr][c] - m[rr]);
+          l[rr] += pv[nb][rr][c];
         }
     }
-    float pv[KW / 8][2];
-#pragma unroll
-    for (int nb = 0; nb < KW / 8; ++nb)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        pv[nb][c] = sv[nb][c] == -INFINITY ? 0.f : ex2(sv[nb][c] - m);
-        l += pv[nb][c];
-      }
     // ---- O += P V
     const uint8_t* r0 = vs + (warp * KW + 2 * t) * kRowBytes;  // key 2t of this warp's keys
     if constexpr (kBytes == 2) {
-      const uint32_t a0 = pack_bf16x2(pv[0][0], pv[0][1]);
+      const uint32_t a0 = pack_bf16x2(pv[0][0][0], pv[0][0][1]);
+      const uint32_t a1 = kTwoRows ? pack_bf16x2(pv[0][NR - 1][0], pv[0][NR - 1][1]) : 0u;
 #pragma unroll
       for (int b = 0; b < SB; ++b) {
         const uint2 x = *reinterpret_cast<const uint2*>(r0 + 2 * (32 * b + 4 * g));
         const uint2 y = *reinterpret_cast<const uint2*>(r0 + kRowBytes + 2 * (32 * b + 4 * g));
-        mma_1688_bf16(o[b][0], a0, __byte_perm(x.x, y.x, 0x5410));
-        mma_1688_bf16(o[b][1], a0, __byte_perm(x.x, y.x, 0x7632));
-        mma_1688_bf16(o[b][2], a0, __byte_perm(x.y, y.y, 0x5410));
-        mma_1688_bf16(o[b][3], a0, __byte_perm(x.y, y.y, 0x7632));
+        const uint32_t bj[4] = {__byte_perm(x.x, y.x, 0x5410), __byte_perm(x.x, y.x, 0x7632),
+                                __byte_perm(x.y, y.y, 0x5410), __byte_perm(x.y, y.y, 0x7632)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          asm volatile(
+              "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+              "{%0,%1,%2,%3};"
+              : "+f"(o[b][j][0]), "+f"(o[b][j][1]), "+f"(o[b][j][2]), "+f"(o[b][j][3])
+              : "r"(a0), "r"(a1), "r"(bj[j]));
       }
     } else {
-      const uint32_t a0 = pack_f16x2(pv[0][0], pv[0][1]), a2 = pack_f16x2(pv[1][0], pv[1][1]);
+      const uint32_t a0 = pack_f16x2(pv[0][0][0], pv[0][0][1]), a2 = pack_f16x2(pv[1][0][0], pv[1][0][1]);
+      const uint32_t a1 = kTwoRows ? pack_f16x2(pv[0][NR - 1][0], pv[0][NR - 1][1]) : 0u;
+      const uint32_t a3 = kTwoRows ? pack_f16x2(pv[1][NR - 1][0], pv[1][NR - 1][1]) : 0u;
 #pragma unroll
       for (int b = 0; b < SB; ++b) {
         const int col = 32 * b + 4 * g;
@@ -588,29 +633,40 @@ struct MmaState {
         const uint32_t y1 = *reinterpret_cast<const uint32_t*>(r0 + 9 * kRowBytes + col);
         const uint32_t xa = __byte_perm(x0, x1, 0x5140), xb = __byte_perm(x0, x1, 0x7362);
         const uint32_t ya = __byte_perm(y0, y1, 0x5140), yb = __byte_perm(y0, y1, 0x7362);
-        mma_16816_f16(o[b][0], a0, a2, e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(ya));
-        mma_16816_f16(o[b][1], a0, a2, e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(ya >> 16));
-        mma_16816_f16(o[b][2], a0, a2, e4m3x2_to_f16x2(xb), e4m3x2_to_f16x2(yb));
-        mma_16816_f16(o[b][3], a0, a2, e4m3x2_to_f16x2(xb >> 16), e4m3x2_to_f16x2(yb >> 16));
+        const uint32_t b0[4] = {e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(xb),
+                                e4m3x2_to_f16x2(xb >> 16)};
+        const uint32_t b1[4] = {e4m3x2_to_f16x2(ya), e4m3x2_to_f16x2(ya >> 16), e4m3x2_to_f16x2(yb),
+                                e4m3x2_to_f16x2(yb >> 16)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          asm volatile(
+              "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+              "{%8,%9}, {%0,%1,%2,%3};"
+              : "+f"(o[b][j][0]), "+f"(o[b][j][1]), "+f"(o[b][j][2]), "+f"(o[b][j][3])
+              : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0[j]), "r"(b1[j]));
       }
     }
   }
   SGL_DEV void publish(float* red_acc, float* red_m, float* red_l) {
-    float ls = l;
-    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-    if (g < G) {
-      float* dst = red_acc + (warp * G + g) * D + 8 * t;
 #pragma unroll
-      for (int b = 0; b < SB; ++b)
+    for (int rr = 0; rr < NR; ++rr) {
+      float ls = l[rr];
+      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+      const int row = g + 8 * rr;
+      if (row < G) {
+        float* dst = red_acc + (warp * G + row) * D + 8 * t;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          dst[32 * b + j] = o[b][j][0];
-          dst[32 * b + 4 + j] = o[b][j][1];
+        for (int b = 0; b < SB; ++b)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            dst[32 * b + j] = o[b][j][2 * rr];
+            dst[32 * b + 4 + j] = o[b][j][2 * rr + 1];
+          }
+        if (t == 0) {
+          red_m[warp * G + row] = m[rr];
+          red_l[warp * G + row] = ls;
         }
-      if (t == 0) {
-        red_m[warp * G + g] = m;
-        red_l[warp * G + g] = ls;
       }
     }
   }
@@ -826,6 +882,11 @@ sgl_status run_g(int G, const Params& prm, int64_t max_items, const Groups& gr,
     case 2: return run<D, 2, KV>(prm, max_items, gr, ga, stream);
     case 4: return run<D, 4, KV>(prm, max_items, gr, ga, stream);
     case 8: return run<D, 8, KV>(prm, max_items, gr, ga, stream);
+    case 3: return run<D, 3, KV>(prm, max_items, gr, ga, stream);
+    case 5: return run<D, 5, KV>(prm, max_items, gr, ga, stream);
+    case 6: return run<D, 6, KV>(prm, max_items, gr, ga, stream);
+    case 7: return run<D, 7, KV>(prm, max_items, gr, ga, stream);
+    case 16: return run<D, 16, KV>(prm, max_items, gr, ga, stream);
     default: return SGL_ERR_UNSUPPORTED;
   }
 }
@@ -843,7 +904,7 @@ size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, in
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.batch == 0) return SGL_OK;
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return SGL_ERR_UNSUPPORTED;
+  if (!((G >= 1 && G <= 8) || G == 16)) return SGL_ERR_UNSUPPORTED;
   const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);

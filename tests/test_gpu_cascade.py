@@ -54,6 +54,8 @@ TREES = [
     (32, 4, 128, (3, 2), (1, 200), (0, 3)),
     (16, 8, 128, (1, 150), (100, 700), (0, 600)),   # one group of 150 members
     (4, 2, 64, (2, 2, 2), (120, 140), (0, 1)),      # g = 2, D = 64
+    (12, 2, 128, (2, 3), (40, 300), (0, 50)),        # g = 6
+    (32, 2, 128, (3, 2), (10, 200), (1, 30)),        # g = 16
 ]
 
 

@@ -99,6 +99,13 @@ DECODE_SHAPES = [
     (8, 1, 128, [600, 1]),
     (16, 2, 64, [530, 64]),
     (4, 1, 64, [1500]),
+    # group sizes without a CUDA-core build: tensor-core rows (3, 5, 6, 7; 16 uses rows 8..15)
+    (6, 2, 128, [700, 1, 33]),
+    (10, 2, 128, [1500, 17]),
+    (12, 2, 64, [300, 2049]),
+    (28, 4, 128, [1025, 64]),
+    (32, 2, 128, [900, 1, 4100]),
+    (16, 1, 64, [513]),
 ]
 
 
