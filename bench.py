@@ -346,6 +346,34 @@ def small_kwargs(args):
     return SMALL.get(args.config, {}) if getattr(args, "small", False) else {}
 
 
+def prefix_sharing(rows):
+    """Batch cache hit rate ("Origins: the paper and the first commit", the
+    paper's notation table: hit rate = 1 - C / prompt tokens, C = the summed
+    edge lengths of the batch's radix tree), from the library's radix tree with
+    every row's slots inserted as its tokens."""
+    from radixattention_prefix_shared_gb300 import binding as B
+    tree = B.RadixTree()
+    total = 0
+    for row in rows:
+        tree.insert(row, row)
+        total += len(row)
+    unique = tree.evictable_tokens
+    return {"prompt_tokens": int(total), "tree_tokens": int(unique),
+            "hit_rate": round(1.0 - unique / total, 4) if total else 0.0}
+
+
+def sharing_of(w: W.Workload):
+    out = {}
+    if w.extend is not None:
+        e = w.extend
+        out["extend"] = prefix_sharing([w.req_to_token[r, : p + n] for r, p, n in
+                                        zip(e.req_pool_idx, e.prefix_lens, e.extend_lens)])
+    if w.decode:
+        b = w.decode[0]
+        out["decode"] = prefix_sharing([w.req_to_token[r, :n] for r, n in zip(b.req_pool_idx, b.seq_lens)])
+    return out
+
+
 def work_of(w: W.Workload, groups=(), kv_elem_bytes=2):
     d = w.dims
     flops = 0
@@ -538,6 +566,7 @@ def gpu_arm(args):
                    "decode_path": ("cascade" if step.cascade else "plain") if w.decode else None,
                    "launch": "cuda_graph" if graph is not None else "eager",
                    "kv_cache_dtype": "fp8_e4m3" if step.fp8 else "bf16",
+                   "prefix_sharing": sharing_of(w),
                    "l2": "flushed between steps (256 MiB write)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_bytes),
                 "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": round(e_ms, 4),

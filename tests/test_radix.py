@@ -122,3 +122,26 @@ def test_a_tree_built_batch_feeds_cascade_decode():
     casc = oracle.cascade_decode_attention(q, k, v, rows, rpi, sl, cg.group_start, cg.group_len, cg.group_depth,
                                            cg.member_off, cg.members, 2, 0.25)
     assert live.size > 0 and np.max(np.abs(plain - casc)) < 1e-12
+
+
+def test_tree_tokens_give_the_batch_hit_rate():
+    """The paper's notation: hit rate = 1 - C / prompt tokens with C the summed
+    edge lengths of the batch's radix tree -- brute force: C is the number of
+    distinct token prefixes of the batch."""
+    import bench
+    rng = np.random.default_rng(13)
+    stems, rows = [], []
+    for _ in range(60):
+        s = _seq(rng, stems, 4)
+        stems.append(s)
+        rows.append(np.asarray(s, np.int32))
+    got = bench.prefix_sharing(rows)
+    distinct = {tuple(r[: i + 1].tolist()) for r in rows for i in range(len(r))}
+    total = sum(len(r) for r in rows)
+    assert got["tree_tokens"] == len(distinct) and got["prompt_tokens"] == total
+    assert abs(got["hit_rate"] - (1 - len(distinct) / total)) < 1e-4
+    # a tree workload (depth 3, fan-out 2, 16-token segments): 2 + 4 + 8 segments, each
+    # cached once, plus one new token per leaf
+    w = W.tree_of_thought_decode(depth=3, fanout=2, segment=16, steps=1, pool_size=1 << 12)
+    sh = bench.sharing_of(w)["decode"]
+    assert sh["tree_tokens"] == (2 + 4 + 8) * 16 + 8 and sh["prompt_tokens"] == 8 * (3 * 16 + 1)
