@@ -359,7 +359,7 @@ def prefix_sharing(rows):
         total += len(row)
     unique = tree.evictable_tokens
     return {"prompt_tokens": int(total), "tree_tokens": int(unique),
-            "hit_rate": round(1.0 - unique / total, 4) if total else 0.0}
+            "within_batch_hit_rate": round(1.0 - unique / total, 4) if total else 0.0}
 
 
 def sharing_of(w: W.Workload):
@@ -368,6 +368,9 @@ def sharing_of(w: W.Workload):
         e = w.extend
         out["extend"] = prefix_sharing([w.req_to_token[r, : p + n] for r, p, n in
                                         zip(e.req_pool_idx, e.prefix_lens, e.extend_lens)])
+        # tokens whose KV the step reads from the cache instead of computing
+        out["extend"]["cached_prefix_fraction"] = round(
+            float(e.prefix_lens.sum()) / max(1.0, float(e.prefix_lens.sum() + e.extend_lens.sum())), 4)
     if w.decode:
         b = w.decode[0]
         out["decode"] = prefix_sharing([w.req_to_token[r, :n] for r, n in zip(b.req_pool_idx, b.seq_lens)])

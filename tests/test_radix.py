@@ -139,7 +139,7 @@ def test_tree_tokens_give_the_batch_hit_rate():
     distinct = {tuple(r[: i + 1].tolist()) for r in rows for i in range(len(r))}
     total = sum(len(r) for r in rows)
     assert got["tree_tokens"] == len(distinct) and got["prompt_tokens"] == total
-    assert abs(got["hit_rate"] - (1 - len(distinct) / total)) < 1e-4
+    assert abs(got["within_batch_hit_rate"] - (1 - len(distinct) / total)) < 1e-4
     # a tree workload (depth 3, fan-out 2, 16-token segments): 2 + 4 + 8 segments, each
     # cached once, plus one new token per leaf
     w = W.tree_of_thought_decode(depth=3, fanout=2, segment=16, steps=1, pool_size=1 << 12)
