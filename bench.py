@@ -164,10 +164,13 @@ def barrier():
 class Step:
     """Device buffers of one workload and the launches of one step."""
 
-    def __init__(self, w: W.Workload, device, cascade: str = "off", kv: str = "bf16"):
+    def __init__(self, w: W.Workload, device, cascade: str = "off", kv: str = "bf16",
+                 overlap: bool = False):
         import torch
         from radixattention_prefix_shared_gb300 import binding as B
         self.B, self.torch, self.w, self.dev = B, torch, w, device
+        self.overlap = overlap
+        self.side = torch.cuda.Stream(device=device) if overlap else None
         t = W.to_device(w, device)
         self.t = t
         self.fp8 = kv == "fp8"
@@ -238,8 +241,14 @@ class Step:
         self.launches = 0
 
     def run(self, ev=None):
-        """One step; records events [start, after store, after extend, after decode]."""
+        """One step; records events [start, after store, after extend, after decode].
+
+        With `overlap` (and no events) the extend and the decode batches, which
+        touch different requests, run on two streams after the store and join
+        before the step ends: the decode CTAs take the SMs the extend's last
+        wave leaves idle."""
         B, t, w = self.B, self.t, self.w
+        torch = self.torch
         launches = 0
         if ev is not None:
             ev[0].record()
@@ -247,6 +256,27 @@ class Step:
         launches += 1
         if ev is not None:
             ev[1].record()
+        fork = self.overlap and ev is None and w.extend is not None and bool(w.decode)
+        if fork:
+            main = torch.cuda.current_stream()
+            self.side.wait_stream(main)
+            with torch.cuda.stream(self.side):
+                launches += self.run_extend()
+            launches += self.run_decode()
+            main.wait_stream(self.side)
+            self.launches = launches
+            return
+        launches += self.run_extend()
+        if ev is not None:
+            ev[2].record()
+        launches += self.run_decode()
+        if ev is not None:
+            ev[3].record()
+        self.launches = launches
+
+    def run_extend(self):
+        B, t, w = self.B, self.t, self.w
+        launches = 0
         if w.extend is not None:
             e, te = w.extend, t["extend"]
             B.sgl_extend_attention(te["q"], te["k_new"], te["v_new"], t["pool_k"], t["pool_v"],
@@ -254,8 +284,11 @@ class Step:
                                    te["extend_lens"], self.out_ext, max_extend=int(e.extend_lens.max()),
                                    max_prefix=int(e.prefix_lens.max()), workspace=self.ws_ext)
             launches += 1
-        if ev is not None:
-            ev[2].record()
+        return launches
+
+    def run_decode(self):
+        B, t, w = self.B, self.t, self.w
+        launches = 0
         for s, (b, tb) in enumerate(zip(w.decode, t["decode"])):
             if s > 0:
                 self.store(tb["k_new"], tb["v_new"], tb["slots"])
@@ -279,9 +312,7 @@ class Step:
                                        tb["req_pool_idx"], tb["seq_lens"], self.out_dec[s],
                                        max_seq_len=int(b.seq_lens.max()), workspace=self.ws_dec[s])
                 launches += 3                        # plan, split, combine
-        if ev is not None:
-            ev[3].record()
-        self.launches = launches
+        return launches
 
     def store(self, k, v, slots):
         t = self.t
@@ -423,7 +454,7 @@ def gpu_arm(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.make(args.config, seed=1000 + args.config + 7919 * rank, **small_kwargs(args))
-    step = Step(w, dev, args.cascade, args.kv)
+    step = Step(w, dev, args.cascade, args.kv, overlap=args.overlap == "on")
     work = work_of(w, step.groups, 1 if step.fp8 else 2)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x L2
     stream = torch.cuda.current_stream()
@@ -568,6 +599,7 @@ def gpu_arm(args):
                    "query_tokens_per_step": int(step.tokens), "parallelism": f"replicas{world}",
                    "decode_path": ("cascade" if step.cascade else "plain") if w.decode else None,
                    "launch": "cuda_graph" if graph is not None else "eager",
+                   "extend_decode_overlap": step.overlap,
                    "kv_cache_dtype": "fp8_e4m3" if step.fp8 else "bf16",
                    "prefix_sharing": sharing_of(w),
                    "l2": "flushed between steps (256 MiB write)"},
@@ -694,6 +726,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="KV pool element type (fp8: e4m3 codes with per-tensor scales; decode-only workloads)")
+    ap.add_argument("--overlap", choices=["on", "off"], default="on",
+                    help="run the extend and the decode batches of a step on two streams")
     ap.add_argument("--graph", choices=["on", "off"], default="on",
                     help="time the step replayed as one CUDA graph (per-kernel times stay eager)")
     ap.add_argument("--cascade", choices=["auto", "on", "off"], default="auto",
