@@ -24,8 +24,9 @@ What it computes, and where the pages fix it:
     slot numbers in the rows ("Inside SGLang", Step 3: Paged KV and the
     kernels that read it).
   * FP8 KV pool (``oracle.fp8``): e4m3 codes with one scale per tensor,
-    quantised from the float32 quotient x / scale, decode over the
-    dequantised rows -- "Inside SGLang", Step 6 (Decide how much memory
+    quantised from the float32 quotient x / scale; decode, extend (suffix
+    rows read back from the pool like the prefix) and cascade decode over
+    the dequantised rows -- "Inside SGLang", Step 6 (Decide how much memory
     becomes KV cache: --kv-cache-dtype fp8_e4m3, scales from the checkpoint).
   * radix tree (``oracle.radix``): token runs with their KV slots, match
     with node splitting, insert, lock counts on the path to the root,

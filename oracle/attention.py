@@ -186,6 +186,16 @@ def cascade_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_
     member's row agrees with its group's first member over the group's range,
     this equals ``decode_attention``.  Returns [B, Hq, D] (or the listed
     requests)."""
+    return _cascade_decode(q, lambda slots: (bf16_bits_to_f64(pool_k[slots]), bf16_bits_to_f64(pool_v[slots])),
+                           req_to_token, req_pool_idx, seq_lens, group_start, group_len, group_depth,
+                           member_off, members, num_kv_heads, sm_scale, requests)
+
+
+def _cascade_decode(q, read_kv, req_to_token, req_pool_idx, seq_lens, group_start, group_len,
+                    group_depth, member_off, members, num_kv_heads, sm_scale, requests):
+    """``cascade_decode_attention`` with the pool read through
+    ``read_kv(slots) -> (K, V)`` (float64 rows) so that the e4m3 pool's
+    variant shares the grouping."""
     q = np.asarray(q)
     B, Hq, D = q.shape
     scale = default_scale(D) if sm_scale is None else float(sm_scale)
@@ -209,11 +219,9 @@ def cascade_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_
         for _, j in sorted(mine[r]):
             first = int(members[member_off[j]])
             a, e = int(group_start[j]), int(group_start[j] + group_len[j])
-            slots = np.asarray(req_to_token[int(req_pool_idx[first]), a:e], np.int64)
-            pieces.append((bf16_bits_to_f64(pool_k[slots]), bf16_bits_to_f64(pool_v[slots])))
+            pieces.append(read_kv(np.asarray(req_to_token[int(req_pool_idx[first]), a:e], np.int64)))
             shared = e
-        slots = np.asarray(req_to_token[int(req_pool_idx[r]), shared:int(seq_lens[r])], np.int64)
-        pieces.append((bf16_bits_to_f64(pool_k[slots]), bf16_bits_to_f64(pool_v[slots])))
+        pieces.append(read_kv(np.asarray(req_to_token[int(req_pool_idx[r]), shared:int(seq_lens[r])], np.int64)))
         for h in range(Hq):
             kh = _kv_head_of(h, Hq, num_kv_heads)
             out[n, h] = merge_states([partial_state(qr[h], K[:, kh], V[:, kh], scale)

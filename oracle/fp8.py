@@ -12,6 +12,10 @@ Readings taken where the page leaves a step open:
     finite value 448;
   * one scale per tensor (K and V separately); a stored code c stands for
     ``decode(c) * scale``;
+  * every key and value an attention over an e4m3 pool reads comes from the
+    pool: an EXTEND's suffix rows are stored (quantised) before it runs and
+    read back through ``req_to_token`` like its prefix, so extend, decode and
+    cascade decode all see the same dequantised values for a position;
   * quantising takes the float32 quotient ``x / scale`` (IEEE division,
     round to nearest even) and rounds it to e4m3 to nearest, ties to even,
     saturating to +-448 (finite inputs never become NaN).
@@ -20,7 +24,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import _kv_head_of, _softmax_attend, bf16_bits_to_f64, default_scale
+from .attention import (_cascade_decode, _kv_head_of, _softmax_attend, _visible_keys, bf16_bits_to_f64,
+                        default_scale)
 
 E4M3_MAX = 448.0
 
@@ -103,3 +108,55 @@ def decode_attention_fp8(q, pool_k, pool_v, k_scale: float, v_scale: float, req_
             kh = _kv_head_of(h, Hq, num_kv_heads)
             out[n, h] = _softmax_attend(qr[h], K[:, kh], V[:, kh], scale)
     return out
+
+
+def _dequant(codes, scale: float) -> np.ndarray:
+    return e4m3_decode(codes) * float(scale)
+
+
+def extend_attention_fp8(q, pool_k, pool_v, k_scale: float, v_scale: float, req_to_token,
+                         req_pool_idx, prefix_lens, extend_lens, num_kv_heads: int, sm_scale=None,
+                         tokens=None) -> np.ndarray:
+    """EXTEND attention over an e4m3 pool, float64.
+
+    q [T, Hq, D] holds the suffix queries of all requests back to back
+    (request r's rows start at the exclusive prefix sum of extend_lens).
+    Request r's keys and values are its row ``req_to_token[req_pool_idx[r],
+    0 : p + e]`` -- cached prefix and freshly stored suffix alike --
+    dequantised; suffix query i (position p + i) attends to keys 0 .. p + i,
+    as in ``extend_attention``.  Returns [T, Hq, D] (or the listed rows)."""
+    q = np.asarray(q)
+    T, Hq, D = q.shape
+    scale = default_scale(D) if sm_scale is None else float(sm_scale)
+    prefix_lens = np.asarray(prefix_lens, dtype=np.int64)
+    extend_lens = np.asarray(extend_lens, dtype=np.int64)
+    offs = np.concatenate([[0], np.cumsum(extend_lens)])
+    want = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    out = np.zeros((want.size, Hq, D), np.float64)
+    req_of = np.searchsorted(offs, want, side="right") - 1
+    for r in np.unique(req_of):
+        p, e, o = int(prefix_lens[r]), int(extend_lens[r]), int(offs[r])
+        slots = np.asarray(req_to_token[int(req_pool_idx[r]), : p + e], dtype=np.int64)
+        K = _dequant(pool_k[slots], k_scale)         # [p+e, Hkv, D]
+        V = _dequant(pool_v[slots], v_scale)
+        for n in np.nonzero(req_of == r)[0]:
+            i = int(want[n]) - o
+            L = _visible_keys(p, i)
+            qi = bf16_bits_to_f64(q[o + i])
+            for h in range(Hq):
+                kh = _kv_head_of(h, Hq, num_kv_heads)
+                out[n, h] = _softmax_attend(qi[h], K[:L, kh], V[:L, kh], scale)
+    return out
+
+
+def cascade_decode_attention_fp8(q, pool_k, pool_v, k_scale: float, v_scale: float, req_to_token,
+                                 req_pool_idx, seq_lens, group_start, group_len, group_depth,
+                                 member_off, members, num_kv_heads: int, sm_scale=None,
+                                 requests=None) -> np.ndarray:
+    """``cascade_decode_attention`` over an e4m3 pool: each group's keys (read
+    once, from its first member's row) and each request's private tail are
+    dequantised (``decode(code) * scale``) before the softmax states are
+    formed and merged."""
+    return _cascade_decode(q, lambda slots: (_dequant(pool_k[slots], k_scale), _dequant(pool_v[slots], v_scale)),
+                           req_to_token, req_pool_idx, seq_lens, group_start, group_len, group_depth,
+                           member_off, members, num_kv_heads, sm_scale, requests)

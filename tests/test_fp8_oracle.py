@@ -9,7 +9,12 @@
   * invariant: decode over an e4m3 pool equals the (pinned) bf16 decode over
     the same values held in bf16, which holds every e4m3 value exactly
     ("Inside SGLang", Step 6: --kv-cache-dtype fp8_e4m3 halves the bytes of
-    each token; K and V carry one scale each).
+    each token; K and V carry one scale each);
+  * the same invariant for extend (against the pinned bf16 extend, whose
+    suffix keys are the rows stored at the suffix slots) and for cascade
+    decode (against the pinned bf16 cascade and the FP8 decode);
+  * cross-function: the last suffix row of an FP8 extend equals an FP8
+    decode of the same query over the same row.
 """
 import numpy as np
 import pytest
@@ -19,7 +24,7 @@ import oracle
 from oracle import fp8 as F
 from radixattention_prefix_shared_gb300 import workloads as W
 
-from _cases import decode_case
+from _cases import decode_case, extend_case
 
 
 def _torch_decode(codes):
@@ -123,3 +128,87 @@ def test_pins_catch_planted_encoder_slips(slip, monkeypatch):
     bad = (lambda v: np.floor(v + 0.5)) if slip == "ties away from zero" else np.floor
     monkeypatch.setattr(F, "_round_half_even", bad)
     assert not np.array_equal(F.e4m3_encode(x), want), f"planted slip '{slip}' not caught"
+
+
+def _exact_pools(w, decode_steps, k_scale, v_scale):
+    """e4m3 pools of a small workload and the same values held exactly in bf16
+    (power-of-two scales keep code * scale exact)."""
+    pk, pv = w.dense_pools(decode_steps=decode_steps)
+    pk[pk == W.BF16_NAN] = 0
+    pv[pv == W.BF16_NAN] = 0
+    qk, qv = F.quantize(pk, k_scale), F.quantize(pv, v_scale)
+    bk = W.f32_to_bf16_bits((F.e4m3_decode(qk) * k_scale).astype(np.float32))
+    bv = W.f32_to_bf16_bits((F.e4m3_decode(qv) * v_scale).astype(np.float32))
+    if np.log2(k_scale) % 1 == 0 and np.log2(v_scale) % 1 == 0:
+        assert np.array_equal(oracle.bf16_bits_to_f64(bv), F.e4m3_decode(qv) * v_scale)
+    return qk, qv, bk, bv
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.25, 2.0)])
+def test_fp8_extend_equals_bf16_extend_on_the_same_values(k_scale, v_scale):
+    w = extend_case(62, Hq=4, Hkv=2, D=16, prefix_lens=[0, 5, 33, 17], extend_lens=[3, 1, 20, 9],
+                    shares=((2, 3, 11),))
+    e = w.extend
+    qk, qv, bk, bv = _exact_pools(w, 0, k_scale, v_scale)
+    got = F.extend_attention_fp8(e.q, qk, qv, k_scale, v_scale, w.req_to_token, e.req_pool_idx,
+                                 e.prefix_lens, e.extend_lens, 2, w.dims.sm_scale)
+    # the bf16 extend takes the suffix keys from k_new / v_new: here the rows
+    # stored at the suffix slots
+    want = oracle.extend_attention(e.q, bk[e.slots], bv[e.slots], bk, bv, w.req_to_token, e.req_pool_idx,
+                                   e.prefix_lens, e.extend_lens, 2, w.dims.sm_scale)
+    assert np.max(np.abs(got - want)) < 1e-12
+    some = [0, 4, 23, 32]
+    sub = F.extend_attention_fp8(e.q, qk, qv, k_scale, v_scale, w.req_to_token, e.req_pool_idx,
+                                 e.prefix_lens, e.extend_lens, 2, w.dims.sm_scale, tokens=some)
+    assert np.array_equal(sub, got[some])
+
+
+def test_fp8_extend_last_row_is_an_fp8_decode():
+    w = extend_case(63, Hq=6, Hkv=2, D=16, prefix_lens=[7, 0, 40], extend_lens=[5, 12, 1])
+    e = w.extend
+    ks, vs = 0.0173, 0.031
+    qk, qv, _, _ = _exact_pools(w, 0, ks, vs)
+    ext = F.extend_attention_fp8(e.q, qk, qv, ks, vs, w.req_to_token, e.req_pool_idx, e.prefix_lens,
+                                 e.extend_lens, 2, w.dims.sm_scale)
+    last = np.cumsum(e.extend_lens) - 1
+    dec = F.decode_attention_fp8(e.q[last], qk, qv, ks, vs, w.req_to_token, e.req_pool_idx,
+                                 e.prefix_lens + e.extend_lens, 2, w.dims.sm_scale)
+    assert np.max(np.abs(ext[last] - dec)) < 1e-12
+    # an earlier row sees fewer keys: it differs from the decode over the whole row
+    assert np.max(np.abs(ext[last - 1][2] - dec[2])) > 1e-3
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.5, 0.125)])
+def test_fp8_cascade_equals_bf16_cascade_and_fp8_decode(k_scale, v_scale):
+    dims = W.Dims(4, 2, 16, 1 << 14, 0.25)
+    w = W.random_tree_decode(seed=21, dims=dims, pool_size=1 << 14, fanouts=(2, 3), seg_len=(1, 40))
+    cg = W.tree_groups(w)
+    b = w.decode[0]
+    qk, qv, bk, bv = _exact_pools(w, 1, k_scale, v_scale)
+    args = (w.req_to_token, b.req_pool_idx, b.seq_lens, cg.group_start, cg.group_len, cg.group_depth,
+            cg.member_off, cg.members, 2, dims.sm_scale)
+    got = F.cascade_decode_attention_fp8(b.q, qk, qv, k_scale, v_scale, *args)
+    assert np.max(np.abs(got - oracle.cascade_decode_attention(b.q, bk, bv, *args))) < 1e-12
+    dec = F.decode_attention_fp8(b.q, qk, qv, k_scale, v_scale, w.req_to_token, b.req_pool_idx, b.seq_lens,
+                                 2, dims.sm_scale)
+    assert cg.n_groups > 0 and np.max(np.abs(got - dec)) < 1e-12
+
+
+@pytest.mark.parametrize("slip", ["suffix read one position late", "V scale dropped"])
+def test_pins_catch_planted_extend_slips(slip, monkeypatch):
+    if slip == "V scale dropped":
+        monkeypatch.setattr(F, "_dequant", lambda codes, scale: F.e4m3_decode(codes) * (scale if scale != 2.0 else 1.0))
+        case = lambda: test_fp8_extend_equals_bf16_extend_on_the_same_values(0.25, 2.0)  # noqa: E731
+    else:
+        real = F.extend_attention_fp8
+
+        def sloppy(q, pool_k, pool_v, ks, vs, rtt, rpi, pl, el, hkv, sc=None, tokens=None):
+            # the suffix read from the row one position late
+            rtt = np.array(rtt, copy=True)
+            for r, p, e in zip(rpi, pl, el):
+                rtt[r, p: p + e] = rtt[r, p + 1: p + e + 1]
+            return real(q, pool_k, pool_v, ks, vs, rtt, rpi, pl, el, hkv, sc, tokens)
+        monkeypatch.setattr(F, "extend_attention_fp8", sloppy)
+        case = test_fp8_extend_last_row_is_an_fp8_decode
+    with pytest.raises(AssertionError):
+        case()
