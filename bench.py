@@ -175,8 +175,6 @@ class Step:
         self.t = t
         self.fp8 = kv == "fp8"
         if self.fp8:
-            if w.extend is not None:
-                raise SystemExit("--kv fp8: extend over an e4m3 pool is not built; use a decode-only workload")
             # the cached rows pass through the quantising store once (setup);
             # one scale per tensor, as a checkpoint provides
             self.k_scale = self.v_scale = FP8_SCALE
@@ -217,9 +215,7 @@ class Step:
         # off its rows once here (the host side of a serving loop keeps them
         # in its radix tree); "auto" uses them when the batch shares prefixes
         self.groups = []
-        if cascade == "on" and self.fp8:
-            raise SystemExit("--kv fp8: cascade decode over an e4m3 pool is not built")
-        if cascade != "off" and w.decode and not self.fp8:
+        if cascade != "off" and w.decode:
             self.groups = [W.tree_groups(w, s) for s in range(len(w.decode))]
             if cascade == "auto" and not any(g.n_groups for g in self.groups):
                 self.groups = []
@@ -277,7 +273,16 @@ class Step:
     def run_extend(self):
         B, t, w = self.B, self.t, self.w
         launches = 0
-        if w.extend is not None:
+        if w.extend is not None and self.fp8:
+            # the suffix rows were stored (quantised) with the step's store and
+            # are read back from the pool like the prefix
+            e, te = w.extend, t["extend"]
+            B.sgl_extend_attention_fp8(te["q"], t["pool_k"], t["pool_v"], self.k_scale, self.v_scale,
+                                       t["req_to_token"], te["req_pool_idx"], te["prefix_lens"],
+                                       te["extend_lens"], self.out_ext, max_extend=int(e.extend_lens.max()),
+                                       max_prefix=int(e.prefix_lens.max()), workspace=self.ws_ext)
+            launches += 1
+        elif w.extend is not None:
             e, te = w.extend, t["extend"]
             B.sgl_extend_attention(te["q"], te["k_new"], te["v_new"], t["pool_k"], t["pool_v"],
                                    t["req_to_token"], te["req_pool_idx"], te["prefix_lens"],
@@ -299,7 +304,8 @@ class Step:
                                                tb["req_pool_idx"], tb["seq_lens"], *self.groups_dev[s],
                                                self.out_dec[s], max_seq_len=int(b.seq_lens.max()),
                                                max_group_members=max(g.max_members, 1),
-                                               max_depth=max(g.max_depth, 1), workspace=self.ws_dec[s])
+                                               max_depth=max(g.max_depth, 1), workspace=self.ws_dec[s],
+                                               kv_scales=(self.k_scale, self.v_scale) if self.fp8 else None)
                 launches += 4 if g.n_groups else 3   # plan, groups, split, combine
             elif self.fp8:
                 B.sgl_decode_attention_fp8(tb["q"], t["pool_k"], t["pool_v"], self.k_scale, self.v_scale,
@@ -574,18 +580,21 @@ def gpu_arm(args):
     gbs_st = work["store_bytes"] / (ms_store / 1e3) / 1e9
     kernels["store_kv"] = {"ms": round(ms_store, 4), "gbs": round(gbs_st, 1),
                            "algorithmic_gb": round(work["store_bytes"] / 1e9, 4)}
+    # traffic is looked up per workload and pool type (an e4m3 pool's kernels
+    # move other bytes)
     wl = WORKLOAD_NAMES[args.config]
+    tkey = wl + ("_fp8" if step.fp8 else "")
     if "decode" in kernels and (ms_dec >= ms_ext or "extend" not in kernels):
         ach = kernels["decode"]["gbs"]
         roof = {"kernel": "cascade decode (plan + groups + split + combine)" if step.cascade
                 else "decode (plan + split + combine)", "bound": "hbm", "achieved": ach,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                "traffic": measured_traffic("decode", wl), "peak_source": pk["source"]}
+                "traffic": measured_traffic("decode", tkey), "peak_source": pk["source"]}
     else:
         ach = kernels["extend"]["tflops"]
         roof = {"kernel": "extend", "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
-                "traffic": measured_traffic("extend", wl), "peak_source": pk["source"]}
+                "traffic": measured_traffic("extend", tkey), "peak_source": pk["source"]}
     d = w.dims
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -725,7 +734,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
-                    help="KV pool element type (fp8: e4m3 codes with per-tensor scales; decode-only workloads)")
+                    help="KV pool element type (fp8: e4m3 codes with per-tensor scales)")
     ap.add_argument("--overlap", choices=["on", "off"], default="on",
                     help="run the extend and the decode batches of a step on two streams")
     ap.add_argument("--graph", choices=["on", "off"], default="on",

@@ -248,6 +248,22 @@ sgl_status sgl_cascade_decode_attention(
  *   keys and values are code * scale; q, out and the workspace as there
  *   (sgl_decode_workspace_bytes).  The K scale is folded into the query and
  *   the V scale into the output; accumulation is fp32.
+ * sgl_extend_attention_fp8 -- sgl_extend_attention over an e4m3 pool.  Every
+ *   key and value is read from the pool through req_to_token: request r's
+ *   row holds its prefix slots at positions 0..p-1 AND its suffix slots at
+ *   positions p..p+e-1, already written by sgl_store_kv_fp8 (so an extend,
+ *   a later decode and a cascade decode all see the same stored values of a
+ *   position; there is no k_new / v_new argument).  Suffix query i attends to
+ *   positions 0..p+i.  q, out, lengths, workspace as for sgl_extend_attention.
+ *   The codes are widened exactly to f16 tensor-core operands; the query is
+ *   widened from bf16 to f16 (exact for |q| in [2^-14, 65504]; smaller values
+ *   round as f16 subnormals, |q| > 65504 is outside the supported range) and
+ *   P is rounded to f16; accumulation is fp32.  Index check:
+ *   sgl_check_extend_fp8_indices (it covers the suffix positions too).
+ * sgl_cascade_decode_attention_fp8 -- sgl_cascade_decode_attention over an
+ *   e4m3 pool (group pass on f16 tensor-core operands as above, tails and
+ *   combine as sgl_decode_attention_fp8); same arguments, groups, workspace
+ *   (sgl_cascade_decode_workspace_bytes) and preconditions.
  */
 sgl_status sgl_store_kv_fp8(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
                             void* pool_k, void* pool_v, float k_scale, float v_scale,
@@ -259,6 +275,22 @@ sgl_status sgl_decode_attention_fp8(const void* q, const void* pool_k, const voi
                                     int32_t batch, int32_t max_seq_len, void* out, void* workspace,
                                     size_t workspace_bytes, const sgl_attn_dims* dims,
                                     sgl_stream_t stream);
+sgl_status sgl_extend_attention_fp8(const void* q, const void* pool_k, const void* pool_v,
+                                    float k_scale, float v_scale, const int32_t* req_to_token,
+                                    int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                    const int32_t* extend_lens, int32_t batch,
+                                    int32_t total_extend, int32_t max_extend, int32_t max_prefix,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    const sgl_attn_dims* dims, sgl_stream_t stream);
+sgl_status sgl_cascade_decode_attention_fp8(
+    const void* q, const void* pool_k, const void* pool_v, float k_scale, float v_scale,
+    const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+    const int32_t* req_pool_idx, const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+    const int32_t* group_start, const int32_t* group_len, const int32_t* group_depth,
+    const int32_t* group_member_off, const int32_t* group_members, int32_t n_groups,
+    int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
+    size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream);
 
 /* Workspace sizes (host only; no device call). */
 size_t sgl_extend_workspace_bytes(int32_t batch, int32_t total_extend, const sgl_attn_dims* dims);
@@ -288,6 +320,10 @@ size_t sgl_cascade_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, in
  *   kind 10: a request's groups do not cover [0, shared_len) back to back
  *           (two groups at one depth, a gap, or a wrong start)
  *                                            a = request, b = depth, c = group / start
+ * sgl_check_extend_indices checks the slots of positions 0..p-1 of each row
+ * (the ones sgl_extend_attention reads); sgl_check_extend_fp8_indices those
+ * of positions 0..p+e-1 (sgl_extend_attention_fp8 reads the suffix from the
+ * pool too).
  * sgl_check_store_kv_indices needs a scratch bitmap of (pool_size+7)/8 bytes
  * (rounded up to 16) in `bitmap`; it is cleared by the call.
  * sgl_check_cascade_groups needs sgl_check_cascade_scratch_bytes(batch,
@@ -303,6 +339,12 @@ sgl_status sgl_check_extend_indices(const int32_t* req_to_token, int32_t rtt_row
                                     const int32_t* extend_lens, int32_t batch, int32_t total_extend,
                                     int32_t max_extend, int32_t max_prefix, int64_t pool_size,
                                     int32_t* d_error, sgl_stream_t stream);
+sgl_status sgl_check_extend_fp8_indices(const int32_t* req_to_token, int32_t rtt_rows,
+                                        int32_t rtt_stride, const int32_t* req_pool_idx,
+                                        const int32_t* prefix_lens, const int32_t* extend_lens,
+                                        int32_t batch, int32_t total_extend, int32_t max_extend,
+                                        int32_t max_prefix, int64_t pool_size, int32_t* d_error,
+                                        sgl_stream_t stream);
 sgl_status sgl_check_decode_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
                                     const int32_t* req_pool_idx, const int32_t* seq_lens,
                                     int32_t batch, int32_t max_seq_len, int64_t pool_size,

@@ -70,6 +70,15 @@ _SIGS = {
     "sgl_decode_attention_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_f32, c_f32, c_vp, c_i32, c_i32, c_vp,
                                                 c_vp, c_i32, c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims),
                                                 c_vp]),
+    "sgl_extend_attention_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_f32, c_f32, c_vp, c_i32, c_i32, c_vp,
+                                                c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_size,
+                                                _P(sgl_attn_dims), c_vp]),
+    "sgl_cascade_decode_attention_fp8": (ctypes.c_int, [c_vp, c_vp, c_vp, c_f32, c_f32, c_vp, c_i32, c_i32,
+                                                        c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                                        c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_size,
+                                                        _P(sgl_attn_dims), c_vp]),
+    "sgl_check_extend_fp8_indices": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_i32,
+                                                    c_i32, c_i32, c_i64, c_vp, c_vp]),
     "sgl_check_cascade_scratch_bytes": (c_size, [c_i32, c_i32]),
     "sgl_check_cascade_groups": (ctypes.c_int, [c_vp, c_i32, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
                                                 c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_size, c_vp,
@@ -199,8 +208,10 @@ def sgl_check_store_kv_indices(slots, pool_size, d_error, bitmap=None, stream=No
 
 
 def sgl_check_extend_indices(req_to_token, req_pool_idx, prefix_lens, extend_lens, *, total_extend,
-                             max_extend, max_prefix, pool_size, d_error, stream=None):
-    _check("sgl_check_extend_indices", lib().sgl_check_extend_indices(
+                             max_extend, max_prefix, pool_size, d_error, stream=None, fp8=False):
+    """``fp8``: the e4m3 extend's check (suffix positions' slots too)."""
+    name = "sgl_check_extend_fp8_indices" if fp8 else "sgl_check_extend_indices"
+    _check(name, getattr(lib(), name)(
         _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx),
         _ptr(prefix_lens), _ptr(extend_lens), int(req_pool_idx.shape[0]), int(total_extend),
         int(max_extend), int(max_prefix), int(pool_size), _ptr(d_error), _stream(stream)))
@@ -224,12 +235,13 @@ def cascade_decode_workspace_bytes(batch, max_seq_len, max_depth, dims: sgl_attn
 def sgl_cascade_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_lens,
                                  group_start, group_len, group_depth, group_member_off, group_members,
                                  out=None, *, max_seq_len, max_group_members, max_depth,
-                                 workspace=None, sm_scale=0.0, stream=None):
+                                 workspace=None, sm_scale=0.0, stream=None, kv_scales=None):
     """Decode attention with shared-prefix groups read once per group.
 
     ``group_*`` are int32 device tensors (CSR members); ``max_seq_len``,
     ``max_group_members`` and ``max_depth`` are host values.  A new workspace
-    is zero-filled; a reused one must keep its first 256 bytes zero."""
+    is zero-filled; a reused one must keep its first 256 bytes zero.
+    ``kv_scales=(k_scale, v_scale)`` selects the e4m3-pool entry point."""
     import torch
     d = _dims_for(q, pool_k, sm_scale)
     if out is None:
@@ -238,8 +250,13 @@ def sgl_cascade_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, 
     G = int(group_start.shape[0])
     if workspace is None:
         workspace = new_workspace(cascade_decode_workspace_bytes(B, max_seq_len, max_depth, d), q.device)
-    _check("sgl_cascade_decode_attention", lib().sgl_cascade_decode_attention(
-        _ptr(q), _ptr(pool_k), _ptr(pool_v), _ptr(req_to_token), int(req_to_token.shape[0]),
+    if kv_scales is None:
+        name, head = "sgl_cascade_decode_attention", (_ptr(q), _ptr(pool_k), _ptr(pool_v))
+    else:
+        name = "sgl_cascade_decode_attention_fp8"
+        head = (_ptr(q), _ptr(pool_k), _ptr(pool_v), float(kv_scales[0]), float(kv_scales[1]))
+    _check(name, getattr(lib(), name)(
+        *head, _ptr(req_to_token), int(req_to_token.shape[0]),
         int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(seq_lens), B, int(max_seq_len),
         _ptr(group_start), _ptr(group_len), _ptr(group_depth), _ptr(group_member_off), _ptr(group_members),
         G, int(max_group_members), int(max_depth), _ptr(out), _ptr(workspace),
@@ -287,6 +304,27 @@ def sgl_decode_attention_fp8(q, pool_k, pool_v, k_scale, v_scale, req_to_token, 
         int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(seq_lens), B,
         int(max_seq_len), _ptr(out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
         ctypes.byref(d), _stream(stream)))
+    return out
+
+
+def sgl_extend_attention_fp8(q, pool_k, pool_v, k_scale, v_scale, req_to_token, req_pool_idx, prefix_lens,
+                             extend_lens, out=None, *, max_extend, max_prefix=0, total_extend=None,
+                             workspace=None, sm_scale=0.0, stream=None):
+    """Extend attention over an e4m3 pool: prefix AND suffix keys are read
+    from the pool through ``req_to_token`` (the suffix stored first)."""
+    import torch
+    T = int(q.shape[0]) if total_extend is None else int(total_extend)
+    d = _dims_for(q, pool_k, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    B = int(req_pool_idx.shape[0])
+    if workspace is None:
+        workspace = new_workspace(extend_workspace_bytes(B, T, d), q.device)
+    _check("sgl_extend_attention_fp8", lib().sgl_extend_attention_fp8(
+        _ptr(q), _ptr(pool_k), _ptr(pool_v), float(k_scale), float(v_scale), _ptr(req_to_token),
+        int(req_to_token.shape[0]), int(req_to_token.shape[1]), _ptr(req_pool_idx), _ptr(prefix_lens),
+        _ptr(extend_lens), B, T, int(max_extend), int(max_prefix), _ptr(out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), ctypes.byref(d), _stream(stream)))
     return out
 
 

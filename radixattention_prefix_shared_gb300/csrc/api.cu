@@ -60,7 +60,9 @@ __global__ void check_store_kernel(const int32_t* __restrict__ slots, int32_t n,
   }
 }
 
-// mode 0: extend (lens_a = prefix, lens_b = extend); mode 1: decode (lens_a = seq)
+// mode 0: extend (lens_a = prefix, lens_b = extend; the prefix slots are read);
+// mode 2: the same over an e4m3 pool (prefix and suffix slots are read);
+// mode 1: decode (lens_a = seq)
 __global__ void check_rows_kernel(const int32_t* __restrict__ rtt, int32_t rtt_rows, int32_t stride,
                                   const int32_t* __restrict__ rpi, const int32_t* __restrict__ lens_a,
                                   const int32_t* __restrict__ lens_b, int32_t mode, int64_t S,
@@ -72,7 +74,7 @@ __global__ void check_rows_kernel(const int32_t* __restrict__ rtt, int32_t rtt_r
     return;
   }
   int32_t n;
-  if (mode == 0) {
+  if (mode != 1) {
     const int32_t pl = lens_a[r], el = lens_b[r];
     if (pl < 0 || el < 0) {
       if (threadIdx.x == 0) report(err, 3, r, 0, pl < 0 ? pl : el);
@@ -86,7 +88,7 @@ __global__ void check_rows_kernel(const int32_t* __restrict__ rtt, int32_t rtt_r
       if (threadIdx.x == 0) report(err, 5, r, 0, pl > max_a ? pl : el);
       return;
     }
-    n = pl;
+    n = mode == 2 ? pl + el : pl;
   } else {
     const int32_t sl = lens_a[r];
     if (sl < 1) {
@@ -283,24 +285,26 @@ size_t sgl_cascade_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, in
                                 dims->head_dim, true, max_depth);
 }
 
-sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_new,
-                                const void* pool_k, const void* pool_v,
-                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
-                                const int32_t* req_pool_idx, const int32_t* prefix_lens,
-                                const int32_t* extend_lens, int32_t batch, int32_t total_extend,
-                                int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
-                                size_t workspace_bytes, const sgl_attn_dims* dims,
-                                sgl_stream_t stream) {
+namespace {
+// k_new / v_new are null on an e4m3 pool (the suffix is read from the pool)
+sgl_status extend_entry(const void* q, const void* k_new, const void* v_new, const void* pool_k,
+                        const void* pool_v, bool kv_fp8, float k_scale, float v_scale,
+                        const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                        const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                        const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                        int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
+                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
   float scale;
   sgl_status st = check_dims(dims, &scale);
   if (st != SGL_OK) return st;
   if (batch < 0 || total_extend < 0 || max_extend < 0 || max_prefix < 0) return SGL_ERR_INVALID_ARG;
   if (batch == 0 || total_extend == 0) return SGL_OK;
-  if (!q || !k_new || !v_new || !pool_k || !pool_v || !req_to_token || !req_pool_idx ||
-      !prefix_lens || !extend_lens || !out)
+  if (!kv_fp8 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
     return SGL_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) ||
-      !aligned16(pool_v) || !aligned16(out))
+  if (!q || !pool_k || !pool_v || !req_to_token || !req_pool_idx || !prefix_lens || !extend_lens ||
+      !out)
+    return SGL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool_k) || !aligned16(pool_v) || !aligned16(out))
     return SGL_ERR_INVALID_ARG;
   if (rtt_rows <= 0 || rtt_stride <= 0 || max_extend > total_extend) return SGL_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < extend_workspace_bytes() || !aligned16(workspace))
@@ -326,7 +330,40 @@ sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_
   a.num_kv_heads = dims->num_kv_heads;
   a.head_dim = dims->head_dim;
   a.sm_scale = scale;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return launch_extend(a, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+sgl_status sgl_extend_attention(const void* q, const void* k_new, const void* v_new,
+                                const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                                int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
+                                size_t workspace_bytes, const sgl_attn_dims* dims,
+                                sgl_stream_t stream) {
+  if (batch > 0 && total_extend > 0 && (!k_new || !v_new)) return SGL_ERR_INVALID_ARG;
+  return extend_entry(q, k_new, v_new, pool_k, pool_v, false, 1.f, 1.f, req_to_token, rtt_rows,
+                      rtt_stride, req_pool_idx, prefix_lens, extend_lens, batch, total_extend,
+                      max_extend, max_prefix, out, workspace, workspace_bytes, dims, stream);
+}
+
+sgl_status sgl_extend_attention_fp8(const void* q, const void* pool_k, const void* pool_v,
+                                    float k_scale, float v_scale, const int32_t* req_to_token,
+                                    int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                    const int32_t* extend_lens, int32_t batch,
+                                    int32_t total_extend, int32_t max_extend, int32_t max_prefix,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    const sgl_attn_dims* dims, sgl_stream_t stream) {
+  if (!valid_kv_scale(k_scale) || !valid_kv_scale(v_scale)) return SGL_ERR_INVALID_ARG;
+  return extend_entry(q, nullptr, nullptr, pool_k, pool_v, true, k_scale, v_scale, req_to_token,
+                      rtt_rows, rtt_stride, req_pool_idx, prefix_lens, extend_lens, batch,
+                      total_extend, max_extend, max_prefix, out, workspace, workspace_bytes, dims,
+                      stream);
 }
 
 namespace {
@@ -405,12 +442,14 @@ sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, b
 }
 }  // namespace
 
-sgl_status sgl_cascade_decode_attention(
-    const void* q, const void* pool_k, const void* pool_v, const int32_t* req_to_token,
-    int32_t rtt_rows, int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
-    int32_t batch, int32_t max_seq_len, const int32_t* group_start, const int32_t* group_len,
-    const int32_t* group_depth, const int32_t* group_member_off, const int32_t* group_members,
-    int32_t n_groups, int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
+namespace {
+sgl_status cascade_entry(
+    const void* q, const void* pool_k, const void* pool_v, bool kv_fp8, float k_scale,
+    float v_scale, const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+    const int32_t* req_pool_idx, const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+    const int32_t* group_start, const int32_t* group_len, const int32_t* group_depth,
+    const int32_t* group_member_off, const int32_t* group_members, int32_t n_groups,
+    int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
     size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
   float scale;
   sgl_status st = check_dims(dims, &scale);
@@ -459,7 +498,39 @@ sgl_status sgl_cascade_decode_attention(
   a.n_groups = n_groups;
   a.max_group_members = max_group_members;
   a.max_depth = max_depth;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+sgl_status sgl_cascade_decode_attention(
+    const void* q, const void* pool_k, const void* pool_v, const int32_t* req_to_token,
+    int32_t rtt_rows, int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+    int32_t batch, int32_t max_seq_len, const int32_t* group_start, const int32_t* group_len,
+    const int32_t* group_depth, const int32_t* group_member_off, const int32_t* group_members,
+    int32_t n_groups, int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
+    size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+  return cascade_entry(q, pool_k, pool_v, false, 1.f, 1.f, req_to_token, rtt_rows, rtt_stride,
+                       req_pool_idx, seq_lens, batch, max_seq_len, group_start, group_len,
+                       group_depth, group_member_off, group_members, n_groups, max_group_members,
+                       max_depth, out, workspace, workspace_bytes, dims, stream);
+}
+
+sgl_status sgl_cascade_decode_attention_fp8(
+    const void* q, const void* pool_k, const void* pool_v, float k_scale, float v_scale,
+    const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+    const int32_t* req_pool_idx, const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+    const int32_t* group_start, const int32_t* group_len, const int32_t* group_depth,
+    const int32_t* group_member_off, const int32_t* group_members, int32_t n_groups,
+    int32_t max_group_members, int32_t max_depth, void* out, void* workspace,
+    size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+  if (!valid_kv_scale(k_scale) || !valid_kv_scale(v_scale)) return SGL_ERR_INVALID_ARG;
+  return cascade_entry(q, pool_k, pool_v, true, k_scale, v_scale, req_to_token, rtt_rows,
+                       rtt_stride, req_pool_idx, seq_lens, batch, max_seq_len, group_start,
+                       group_len, group_depth, group_member_off, group_members, n_groups,
+                       max_group_members, max_depth, out, workspace, workspace_bytes, dims, stream);
 }
 
 size_t sgl_check_cascade_scratch_bytes(int32_t batch, int32_t max_depth) {
@@ -515,21 +586,42 @@ sgl_status sgl_check_store_kv_indices(const int32_t* slots, int32_t n, int64_t p
   return last_launch();
 }
 
-sgl_status sgl_check_extend_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
-                                    const int32_t* req_pool_idx, const int32_t* prefix_lens,
-                                    const int32_t* extend_lens, int32_t batch, int32_t total_extend,
-                                    int32_t max_extend, int32_t max_prefix, int64_t pool_size,
-                                    int32_t* d_error, sgl_stream_t stream) {
+namespace {
+sgl_status check_extend(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                        const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                        const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                        int32_t max_extend, int32_t max_prefix, int64_t pool_size, int32_t* d_error,
+                        sgl_stream_t stream, int mode) {
   if (batch < 0 || rtt_rows <= 0 || rtt_stride <= 0 || pool_size <= 0 || d_error == nullptr)
     return SGL_ERR_INVALID_ARG;
   if (batch == 0) return SGL_OK;
   if (!req_to_token || !req_pool_idx || !prefix_lens || !extend_lens) return SGL_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   check_rows_kernel<<<(unsigned)batch, 256, 0, s>>>(req_to_token, rtt_rows, rtt_stride, req_pool_idx,
-                                                    prefix_lens, extend_lens, 0, pool_size,
+                                                    prefix_lens, extend_lens, mode, pool_size,
                                                     max_prefix, max_extend, d_error);
   check_sum_kernel<<<1, 1024, 0, s>>>(extend_lens, batch, total_extend, d_error);
   return last_launch();
+}
+}  // namespace
+
+sgl_status sgl_check_extend_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                    const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                                    const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                                    int32_t max_extend, int32_t max_prefix, int64_t pool_size,
+                                    int32_t* d_error, sgl_stream_t stream) {
+  return check_extend(req_to_token, rtt_rows, rtt_stride, req_pool_idx, prefix_lens, extend_lens,
+                      batch, total_extend, max_extend, max_prefix, pool_size, d_error, stream, 0);
+}
+
+sgl_status sgl_check_extend_fp8_indices(const int32_t* req_to_token, int32_t rtt_rows,
+                                        int32_t rtt_stride, const int32_t* req_pool_idx,
+                                        const int32_t* prefix_lens, const int32_t* extend_lens,
+                                        int32_t batch, int32_t total_extend, int32_t max_extend,
+                                        int32_t max_prefix, int64_t pool_size, int32_t* d_error,
+                                        sgl_stream_t stream) {
+  return check_extend(req_to_token, rtt_rows, rtt_stride, req_pool_idx, prefix_lens, extend_lens,
+                      batch, total_extend, max_extend, max_prefix, pool_size, d_error, stream, 2);
 }
 
 sgl_status sgl_check_decode_indices(const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -94,6 +95,25 @@ SGL_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+SGL_DEV uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Four e4m3 codes (byte i = code i) -> two f16x2 words (codes 0,1 and 2,3)
+// holding exactly code * 2^-8.  The f16 bit pattern is the code's sign at
+// bit 15 and its 7 magnitude bits (exponent field e, mantissa m) at bits
+// 7..13: a normal code reads as 2^(e-15) (1 + m/8) = 2^-8 * 2^(e-7) (1 + m/8),
+// a subnormal one (e = 0) as the f16 subnormal m * 2^-17 = 2^-8 * m * 2^-9.
+// (Codes 0x7f / 0xff, e4m3's NaN, read as +-480 * 2^-8; a saturating store
+// never writes them.)
+SGL_DEV void e4m3x4_to_f16x2_scaled(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t hb = ((w >> 1) & 0x3F3F3F3Fu) | (w & 0x80808080u);  // sign | bits 6..1
+  const uint32_t lb = (w << 7) & 0x80808080u;                        // bit 0 -> bit 7
+  lo = __byte_perm(lb, hb, 0x5140);  // (lb0, hb0, lb1, hb1)
+  hi = __byte_perm(lb, hb, 0x7362);  // (lb2, hb2, lb3, hb3)
+}
+
 // ----------------------------------------------------------------- cp.async
 
 // 16-byte global->shared copy through L2 only; src_bytes == 0 writes zeros
@@ -101,6 +121,19 @@ SGL_DEV uint32_t pack_bf16x2(float lo, float hi) {
 SGL_DEV void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
                "r"(src_bytes)
+               : "memory");
+}
+SGL_DEV uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+SGL_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
                : "memory");
 }
 SGL_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -235,15 +268,16 @@ SGL_DEV uint64_t make_sw128_desc(uint32_t smem_addr, uint32_t lbo, uint32_t sbo)
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
-// b_mn_major selects an MN-major (N contiguous) B operand.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4)                            // D format: f32
-         | (1u << 7)                          // A format: bf16
-         | (1u << 10)                         // B format: bf16
-         | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
-         | ((uint32_t)(N >> 3) << 17)         // N / 8
-         | ((uint32_t)(M >> 4) << 24);        // M / 16
+// Instruction descriptor for kind::f16 with bf16 (or, f16_ab, f16) A/B and an
+// fp32 accumulator.  b_mn_major selects an MN-major (N contiguous) B operand.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_major,
+                                                       bool f16_ab = false) {
+  return (1u << 4)                              // D format: f32
+         | ((f16_ab ? 0u : 1u) << 7)            // A format: bf16 (1) or f16 (0)
+         | ((f16_ab ? 0u : 1u) << 10)           // B format: same as A
+         | ((b_mn_major ? 1u : 0u) << 16)       // B major-ness
+         | ((uint32_t)(N >> 3) << 17)           // N / 8
+         | ((uint32_t)(M >> 4) << 24);          // M / 16
 }
 
 // D[tmem] (+)= A[smem] * B[smem]

@@ -293,10 +293,6 @@ SGL_DEV uint32_t e4m3x2_to_f16x2(uint32_t two) {
   const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
   return (uint32_t)r.x | ((uint32_t)r.y << 16);
 }
-SGL_DEV uint32_t pack_f16x2(float a, float b) {
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 template <int D, int G, int LPT>
 __host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
@@ -921,7 +917,6 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // the K scale of an e4m3 pool folds into the query, the V scale into the output
   prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale : 1.f);
   prm.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
-  if (a.kv_fp8 && a.cascade) return SGL_ERR_UNSUPPORTED;
   // cascade: word 0 of the workspace is the group pass's status; the decode
   // scratch follows the status bytes
   const size_t head = a.cascade ? kCascadeStatusBytes : 0;
@@ -962,6 +957,8 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     ga.num_kv_heads = a.num_kv_heads;
     ga.head_dim = a.head_dim;
     ga.sm_scale = a.sm_scale;
+    ga.kv_fp8 = a.kv_fp8;
+    ga.k_scale = a.k_scale;
   }
   const GroupArgs* gp = groups ? &ga : nullptr;
   if (a.kv_fp8) {

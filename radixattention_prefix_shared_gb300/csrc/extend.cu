@@ -38,6 +38,15 @@
 // is rescaled in TMEM, so most blocks need neither a max pass nor a
 // correction pass.
 //
+// e4m3 pool: every key and value -- the suffix too, stored before the call --
+// is gathered through req_to_token as codes.  Four producer warps (one per
+// SM sub-partition) stage the codes with cp.async and widen them to f16 into
+// the swizzled ring with integer ops: the code's seven magnitude bits placed
+// at f16 bit 7 (sign at bit 15) read as exactly code * 2^-8, subnormal codes
+// included, so both MMAs run on f16 operands (the query is widened from bf16,
+// P is packed as f16 with the lazy bound lowered to 2^15) and the 2^8 and the
+// pool's scales fold into the softmax scale and the output.
+//
 // Every wait on an mbarrier is bounded (2 s); on a timeout the kernel raises
 // an abort flag, records a status word in the workspace, drains its own
 // in-flight copies and MMAs, frees TMEM and returns.
@@ -51,16 +60,39 @@ namespace {
 constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per KV block
 constexpr int kSoftmaxWarps = 16;
-constexpr int kProducerWarps = 2;
-constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;  // 18
-constexpr int kThreads = (kMmaWarp + 1) * 32;              // 608
-constexpr int kProducerThreads = kProducerWarps * 32;
-// a producer thread copies 16-byte chunk (ptid % 8) of rows
-// ptid / 8 + kRowStep * i, i < kRowsPerThread, of every 128-row tile
-constexpr int kRowStep = kProducerThreads / 8;
-constexpr int kRowsPerThread = 128 / kRowStep;
-constexpr float kAcceptSum = 4294967296.0f;  // 2^32: largest accepted block row sum
 constexpr uint32_t kTmemCols = 512;
+// e4m3 codes widened by bit placement hold code * 2^-8
+constexpr float kFp8Operand = 256.0f;
+#ifndef SGL_FP8_STAGES
+#define SGL_FP8_STAGES 3
+#endif
+#ifndef SGL_FP8_UNIT_ROWS
+#define SGL_FP8_UNIT_ROWS 128
+#endif
+#ifndef SGL_FP8_RAW_SLOTS
+#define SGL_FP8_RAW_SLOTS 3
+#endif
+#ifndef SGL_FP8_BATCH
+#define SGL_FP8_BATCH 4
+#endif
+
+// warp roles: softmax warps, producer warps, the MMA warp
+// (e4m3: three producer warps, on sub-partitions 0-2 with the MMA warp on
+// the fourth; 20 warps leave 96 registers a thread, 21 would leave 80)
+template <bool kFp8>
+struct Roles {
+  static constexpr int kProducerWarps = kFp8 ? 3 : 2;
+  static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;  // 18 (bf16), 19 (e4m3)
+  static constexpr int kThreads = (kMmaWarp + 1) * 32;              // 608, 640
+  static constexpr int kProducerThreads = kProducerWarps * 32;
+  // a producer thread copies 16-byte chunk (ptid % 8) of the bf16 rows
+  // ptid / 8 + kRowStep * i < 128, i < kRowsPerThread, of every 128-row tile
+  static constexpr int kRowStep = kProducerThreads / 8;
+  static constexpr int kRowsPerThread = (128 + kRowStep - 1) / kRowStep;
+  // largest accepted block row sum: every weight must fit the P operand
+  // (bf16: 2^32; f16: 2^15 < 65504)
+  static constexpr float kAcceptSum = kFp8 ? 32768.0f : 4294967296.0f;
+};
 // TMEM column of S_t and O_t
 SGL_DEV constexpr uint32_t col_s(int t) { return 128u * t; }
 SGL_DEV constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
@@ -70,12 +102,28 @@ SGL_DEV constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 // of every 8 score pairs, this many are exponentiated on the FMA pipe
 constexpr int kFmaExpPairsPer8 = SGL_FMA_EXP_PAIRS_PER8;
 
-template <int D>
+template <int D, bool kFp8>
 struct Cfg {
   static constexpr int kChunks = D / 64;            // 128-byte column chunks per row
   static constexpr int kChunkBytes = 128 * 128;     // 128 rows x 128 bytes
-  static constexpr int kTileBytes = 128 * D * 2;    // Q tile or one K / V block
-  static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots
+  static constexpr int kTileBytes = 128 * D * 2;    // Q tile or one K / V block (16-bit)
+  // K/V ring slots of 16-bit operands (4 keep the next block's K loading
+  // while the current block's last MMAs still read the slot of the one
+  // before: fewer put the widening of K on the tensor core's critical path)
+  static constexpr int kStages = kFp8 ? (D == 128 ? SGL_FP8_STAGES : 2 * SGL_FP8_STAGES)
+                                      : (D == 128 ? 4 : 8);
+  // e4m3: staging slots of raw codes ("units" of kUnitRows rows x D bytes,
+  // unswizzled)
+  static constexpr int kUnitRows = SGL_FP8_UNIT_ROWS;
+  static constexpr int kUnits = 128 / kUnitRows;  // units per tile
+  static constexpr int kRaw = kFp8 ? (D == 128 ? SGL_FP8_RAW_SLOTS : 4) : 0;
+  static constexpr int kRawTileBytes = kUnitRows * D;
+  static constexpr int kRawChunks = D / 16;  // 16-byte code chunks per row
+  static constexpr int kRawRowStep = Roles<kFp8>::kProducerThreads / kRawChunks;
+  static constexpr int kRawRows = (kUnitRows + kRawRowStep - 1) / kRawRowStep;  // rows a thread, per unit
+
+  static_assert(Roles<kFp8>::kProducerThreads % 8 == 0 && Roles<kFp8>::kProducerThreads % kRawChunks == 0,
+                "producer chunk columns");
 };
 
 struct Bars {
@@ -92,20 +140,26 @@ struct Bars {
   float xchg[2][2][128];  // [tile][column half][row]: block maxima, final row sums
 };
 
-// dynamic shared memory: 1024 bytes of alignment slack, Q tiles, the K/V ring, barriers
-template <int D>
+// dynamic shared memory: 1024 bytes of alignment slack, Q tiles, the K/V
+// ring, the raw code staging (e4m3), barriers
+template <int D, bool kFp8>
 constexpr int smem_bytes() {
-  return 1024 + (2 + Cfg<D>::kStages) * Cfg<D>::kTileBytes + (int)sizeof(Bars);
+  using C = Cfg<D, kFp8>;
+  return 1024 + (2 + C::kStages) * C::kTileBytes + C::kRaw * C::kRawTileBytes + (int)sizeof(Bars);
 }
-static_assert(smem_bytes<128>() <= 227 * 1024, "extend kernel shared memory");
-static_assert(smem_bytes<64>() <= 227 * 1024, "extend kernel shared memory");
+static_assert(smem_bytes<128, false>() <= 227 * 1024, "extend kernel shared memory");
+static_assert(smem_bytes<64, false>() <= 227 * 1024, "extend kernel shared memory");
+static_assert(smem_bytes<128, true>() <= 227 * 1024, "extend kernel shared memory");
+static_assert(smem_bytes<64, true>() <= 227 * 1024, "extend kernel shared memory");
 
 struct Params {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_new;
   const __nv_bfloat16* v_new;
-  const __nv_bfloat16* pool_k;
+  const __nv_bfloat16* pool_k;  // bf16 pool
   const __nv_bfloat16* pool_v;
+  const uint8_t* pool_k8;  // e4m3 pool (codes)
+  const uint8_t* pool_v8;
   const int32_t* req_to_token;
   int64_t rtt_stride;
   const int32_t* req_pool_idx;
@@ -114,6 +168,9 @@ struct Params {
   __nv_bfloat16* out;
   int32_t Hq, Hkv, g, tpt, rows_used;
   float scale_log2;
+  // multiplies the normalised output (extend) or the unnormalised P.V rows
+  // (group mode); 1 on a bf16 pool
+  float o_scale;
   int* status;
   // group mode (cascade decode): group j covers positions
   // [group_start[j], group_start[j] + group_len[j]) of its members' rows and
@@ -143,6 +200,178 @@ SGL_DEV bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars, int* status) 
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// Producers on an e4m3 pool (Roles<true>::kProducerThreads threads, ptid =
+// thread index among them; a thread's rows past the tile's end are
+// skipped).  Q: the bf16 rows are copied like on a bf16 pool, then widened to
+// f16 in place.  K/V: each key's D codes are copied with cp.async into an
+// unswizzled staging slot of half a tile (one commit group per half, so a
+// thread waits only for its own copies), widened by bit placement
+// (code * 2^-8 as f16) and stored into the swizzled ring slot; the stores are
+// ordered for the tensor core with a proxy fence before the arrival.  Prefix
+// keys are positions 0..pfx-1 of the request's row, suffix keys positions
+// pfx..pfx+q_end-1 (stored into the pool before the call).
+template <int D, bool kGroup>
+SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* sRaw, Bars* bars,
+                         int ptid, int e, int mbeg, int q0, int pfx, int q_end, int nb_pre, int nb,
+                         int off) {
+  const uint32_t sRaw_a = smem_u32(sRaw);
+  using C = Cfg<D, true>;
+  using R = Roles<true>;
+  const int r = blockIdx.z, kvh = blockIdx.y;
+  // ---- Q tiles (bf16 rows, 16-byte chunk ci of rows rbase + kRowStep * i)
+  const int ci = ptid & 7, rbase = ptid >> 3;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+#pragma unroll
+    for (int i = 0; i < R::kRowsPerThread; ++i) {
+      const int row = rbase + R::kRowStep * i;
+      if (row >= 128) break;
+      const int tok = q0 + t * p.tpt + row / p.g;
+      bool valid = row < p.rows_used && tok < e;
+      int64_t qrow = valid ? (kGroup ? (int64_t)p.members[mbeg + tok] : (int64_t)(off + tok)) : 0;
+      if (kGroup && (qrow < 0 || qrow >= p.batch)) valid = false, qrow = 0;
+      const __nv_bfloat16* src = p.q + (qrow * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + ci * 8;
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c)
+        cp_async_16(sQ_a + t * C::kTileBytes + c * C::kChunkBytes + sw128(row, ci),
+                    valid ? src + c * 64 : p.q, valid ? 16u : 0u);
+    }
+  }
+  cp_async_commit();
+  // ---- K/V codes in units u = kUnits * tile + part (rows kUnitRows * part
+  // ..): 16-byte chunk rc of rows rrow + kRawRowStep * i < kUnitRows
+  const int rc = ptid % C::kRawChunks, rrow = ptid / C::kRawChunks;
+  const int32_t* rtt =
+      kGroup ? p.req_to_token + (int64_t)p.req_pool_idx[p.members[mbeg]] * p.rtt_stride +
+                   p.group_start[r]
+             : p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride;
+  // position of row `row` of block b in the row of req_to_token, or -1 when
+  // the row holds no key (past the prefix, or past this CTA's last query)
+  auto key_pos = [&](int b, int row) {
+    if (b < nb_pre) {
+      const int pos = b * BN + row;
+      return pos < pfx ? pos : -1;
+    }
+    const int j = (b - nb_pre) * BN + row;
+    return j < q_end ? pfx + j : -1;
+  };
+  // the slots of this thread's rows of the next block are loaded one block
+  // ahead (registers), -1 where the row holds no key
+  int32_t slot_cur[C::kUnits][C::kRawRows], slot_next[C::kUnits][C::kRawRows];
+  auto load_slots = [&](int b, int32_t (&dst)[C::kUnits][C::kRawRows]) {
+#pragma unroll
+    for (int h = 0; h < C::kUnits; ++h) {
+#pragma unroll
+      for (int i = 0; i < C::kRawRows; ++i) {
+        const int rr = rrow + C::kRawRowStep * i;
+        const int pos = rr < C::kUnitRows ? key_pos(b, C::kUnitRows * h + rr) : -1;
+        dst[h][i] = pos >= 0 ? rtt[pos] : -1;
+      }
+    }
+  };
+  if (nb > 0) load_slots(0, slot_next);
+  auto issue_raw = [&](int u) {
+    if (u < 2 * C::kUnits * nb) {
+      const int tile = u / C::kUnits, part = u % C::kUnits;
+      const int b = tile >> 1, is_v = tile & 1;
+      if (!is_v && !part) {
+#pragma unroll
+        for (int h = 0; h < C::kUnits; ++h)
+#pragma unroll
+          for (int i = 0; i < C::kRawRows; ++i) slot_cur[h][i] = slot_next[h][i];
+        if (b + 1 < nb) load_slots(b + 1, slot_next);
+      }
+      const uint8_t* pool = is_v ? p.pool_v8 : p.pool_k8;
+      const uint32_t dst0 = sRaw_a + (u % C::kRaw) * C::kRawTileBytes + rc * 16;
+#pragma unroll
+      for (int i = 0; i < C::kRawRows; ++i) {
+        const int rr = rrow + C::kRawRowStep * i;
+        if (rr >= C::kUnitRows) break;
+        const int32_t slot = slot_cur[part][i];
+        const bool valid = slot >= 0;
+        const uint8_t* src = pool + ((int64_t)(valid ? slot : 0) * p.Hkv + kvh) * D + rc * 16;
+        cp_async_16(dst0 + rr * D, src, valid ? 16u : 0u);
+      }
+    }
+    cp_async_commit();  // one group per unit (an empty one past the last)
+  };
+#pragma unroll
+  for (int u = 0; u < C::kRaw; ++u) issue_raw(u);
+  // ---- widen Q in place once its group has landed (the units' groups may not)
+  cp_async_wait<C::kRaw>();
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+#pragma unroll
+    for (int i = 0; i < R::kRowsPerThread; ++i) {
+      const int row = rbase + R::kRowStep * i;
+      if (row >= 128) break;
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        const uint32_t a = sQ_a + t * C::kTileBytes + c * C::kChunkBytes + sw128(row, ci);
+        const uint4 w = ld_shared_v4(a);
+        const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          h[k] = pack_f16x2(__uint_as_float(x[k] << 16), __uint_as_float(x[k] & 0xFFFF0000u));
+        st_shared_v4(a, h[0], h[1], h[2], h[3]);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(&bars->q_full);
+  // ---- widen every K/V tile into the ring, unit by unit
+  bool ok = true;
+  for (int tile = 0; tile < 2 * nb && ok; ++tile) {
+    const int stage = tile % C::kStages, round = tile / C::kStages;
+    if (round > 0) {
+      ok = warp_wait(&bars->kv_empty[stage], (round - 1) & 1, bars, p.status);
+      if (!ok) break;
+    }
+    // codes 16 rc .. 16 rc + 15 of a row are f16 columns of 128-byte chunk
+    // rc / 4, 16-byte pieces 2 (rc % 4) and 2 (rc % 4) + 1.  Plain loads and
+    // stores (not volatile asm) let the compiler issue all of a unit's loads
+    // before the first store; the memory-clobbering cp.async wait above and
+    // copy issue / proxy fence below keep them in place.
+    uint8_t* dst0 = sKV + stage * C::kTileBytes + (rc >> 2) * C::kChunkBytes;
+    const int piece = 2 * (rc & 3);
+#pragma unroll
+    for (int part = 0; part < C::kUnits; ++part) {
+      const int u = C::kUnits * tile + part;
+      cp_async_wait<C::kRaw - 1>();  // this thread's codes of unit u have landed
+      const uint8_t* src0 = sRaw + (u % C::kRaw) * C::kRawTileBytes + rc * 16;
+      constexpr int kBatch = SGL_FP8_BATCH;  // loads in flight per thread
+#pragma unroll
+      for (int i0 = 0; i0 < C::kRawRows; i0 += kBatch) {
+        uint4 w[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int rr = rrow + C::kRawRowStep * (i0 + j);
+          if (i0 + j < C::kRawRows && rr < C::kUnitRows)
+            w[j] = *reinterpret_cast<const uint4*>(src0 + rr * D);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int rr = rrow + C::kRawRowStep * (i0 + j);
+          if (i0 + j >= C::kRawRows || rr >= C::kUnitRows) break;
+          const int row = C::kUnitRows * part + rr;
+          uint4 lo, hi;
+          e4m3x4_to_f16x2_scaled(w[j].x, lo.x, lo.y);
+          e4m3x4_to_f16x2_scaled(w[j].y, lo.z, lo.w);
+          e4m3x4_to_f16x2_scaled(w[j].z, hi.x, hi.y);
+          e4m3x4_to_f16x2_scaled(w[j].w, hi.z, hi.w);
+          *reinterpret_cast<uint4*>(dst0 + sw128(row, piece)) = lo;
+          *reinterpret_cast<uint4*>(dst0 + sw128(row, piece + 1)) = hi;
+        }
+      }
+      issue_raw(u + C::kRaw);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&bars->kv_full[stage]);
+  }
+  cp_async_wait_all();  // nothing of this CTA's shared memory is still being written
+}
+
 // One CTA's work.  Extend mode: (request, KV head, two Q tiles of suffix
 // tokens), keys = the request's prefix from the pool, then its suffix,
 // causally; the normalised output is written as bf16.  Group mode: (shared
@@ -150,15 +379,17 @@ SGL_DEV bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars, int* status) 
 // the members' decode queries and whose keys are the group's positions read
 // once from the first member's row; each row's fp32 softmax state (reference
 // max, row sum, unnormalised P.V) is written for the decode combine to merge.
-template <int D, bool kGroup>
+template <int D, bool kGroup, bool kFp8>
 SGL_DEV void attend_tiles(const Params& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kFp8>;
+  using R = Roles<kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + 2 * C::kTileBytes;
-  Bars* bars = reinterpret_cast<Bars*>(sKV + C::kStages * C::kTileBytes);
+  uint8_t* sRaw = sKV + C::kStages * C::kTileBytes;
+  Bars* bars = reinterpret_cast<Bars*>(sRaw + C::kRaw * C::kRawTileBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // r: the request (extend mode) or the group (group mode); the "tokens" of
@@ -176,13 +407,13 @@ SGL_DEV void attend_tiles(const Params& p) {
   // exclusive prefix sum of extend_lens: where request r's rows start
   if constexpr (!kGroup) {
     int32_t part = 0;
-    for (int i = tid; i < r; i += kThreads) part += p.extend_lens[i];
+    for (int i = tid; i < r; i += R::kThreads) part += p.extend_lens[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) bars->red[warp] = part;
   }
   if (tid == 0) {
-    mbar_init(&bars->q_full, kProducerThreads);
+    mbar_init(&bars->q_full, R::kProducerThreads);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_ready[t], 8 * 32);  // the 8 softmax warps of the tile
@@ -190,13 +421,13 @@ SGL_DEV void attend_tiles(const Params& p) {
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->kv_full[s], kProducerThreads);
+      mbar_init(&bars->kv_full[s], R::kProducerThreads);
       mbar_init(&bars->kv_empty[s], 1);
     }
     bars->abort = 0;
     mbar_fence_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -206,7 +437,7 @@ SGL_DEV void attend_tiles(const Params& p) {
   int32_t off = 0;
   if constexpr (!kGroup) {
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) off += bars->red[w];
+    for (int w = 0; w < R::kThreads / 32; ++w) off += bars->red[w];
   }
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
@@ -264,7 +495,7 @@ SGL_DEV void attend_tiles(const Params& p) {
           }
           if (c & 1) acc1 = fadd2(acc1, pw);
           else acc0 = fadd2(acc0, pw);
-          sr[c] = pack_bf16x2(pw.x, pw.y);
+          sr[c] = kFp8 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
         }
         return (acc0.x + acc0.y) + (acc1.x + acc1.y);
       };
@@ -275,9 +506,9 @@ SGL_DEV void attend_tiles(const Params& p) {
       load_s();
       if (b > 0) {
         // lazy reference: accept the block while this half's row sum stays
-        // <= 2^32 (every weight <= 2^32, safe in fp32 and bf16)
+        // within the bound (every weight then fits the P operand type)
         psum = make_p(m_ref);
-        need = !(psum <= kAcceptSum);
+        need = !(psum <= R::kAcceptSum);
       }
       // The two halves of these rows vote together (one barrier): lane 0 votes
       // "a row of this warp broke the bound", lanes 1-4 vote "this warp gave
@@ -348,18 +579,19 @@ SGL_DEV void attend_tiles(const Params& p) {
           tmem_ld32(tO + (D / 2) * h + 32 * j, o);
           tmem_wait_ld();
           if (wr) {
+            const float os = kFp8 ? p.o_scale : 1.f;
             float4* d4 = reinterpret_cast<float4*>(dst + 32 * j);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              d4[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                  __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+              d4[v] = make_float4(__uint_as_float(o[4 * v]) * os, __uint_as_float(o[4 * v + 1]) * os,
+                                  __uint_as_float(o[4 * v + 2]) * os, __uint_as_float(o[4 * v + 3]) * os);
           }
         }
         if (wr && h == 0) p.part_ml[ent] = make_float2(m_ref, lrow);
       }
     } else if (ok) {
       tc_fence_after();
-      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      const float inv = lrow > 0.f ? (kFp8 ? p.o_scale : 1.f) / lrow : 0.f;
       // this half writes columns [h*D/2, (h+1)*D/2) of the output row
       __nv_bfloat16* orow =
           p.out + ((int64_t)(off + tok) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + (D / 2) * h;
@@ -380,8 +612,13 @@ SGL_DEV void attend_tiles(const Params& p) {
         }
       }
     }
-  } else if (warp < kMmaWarp) {
+  } else if (warp < R::kMmaWarp) {
     // ------------------------------------------------------------ producers
+    if constexpr (kFp8) {
+      produce_fp8<D, kGroup>(p, sQ_a, sKV, sRaw, bars, tid - kSoftmaxWarps * 32, e, mbeg, q0, pfx,
+                             q_end, nb_pre, nb, off);
+    } else {
+    constexpr int kRowStep = R::kRowStep, kRowsPerThread = R::kRowsPerThread;
     const int ptid = tid - kSoftmaxWarps * 32;
     const int ci = ptid & 7;
     const int rbase = ptid >> 3;  // rows rbase + kRowStep * i
@@ -465,10 +702,11 @@ SGL_DEV void attend_tiles(const Params& p) {
       cp_async_mbar_arrive(&bars->kv_full[stage]);
     }
     cp_async_wait_all();  // nothing of this CTA's shared memory is still being written
-  } else if (warp == kMmaWarp && lane == 0) {
+    }
+  } else if (warp == R::kMmaWarp && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idS = make_idesc_bf16(BM, BN, false);
-    constexpr uint32_t idO = make_idesc_bf16(BM, D, true);
+    constexpr uint32_t idS = make_idesc_bf16(BM, BN, false, kFp8);
+    constexpr uint32_t idO = make_idesc_bf16(BM, D, true, kFp8);
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return mbar_wait_bounded(bar, parity, &bars->abort, p.status);
     };
@@ -547,45 +785,57 @@ SGL_DEV void attend_tiles(const Params& p) {
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) extend_kernel(Params p) {
-  attend_tiles<D, false>(p);
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1) extend_kernel(Params p) {
+  attend_tiles<D, false, kFp8>(p);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) cascade_group_kernel(Params p) {
-  attend_tiles<D, true>(p);
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1) cascade_group_kernel(Params p) {
+  attend_tiles<D, true, kFp8>(p);
 }
 
-template <int D>
+template <int D, bool kFp8>
 sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_t stream) {
-  using C = Cfg<D>;
-  auto kern = extend_kernel<D>;
-  if (kernel_blocks_per_sm<extend_kernel<D>>(smem_bytes<D>(), kThreads) < 0) return SGL_ERR_CUDA;
+  constexpr int kThreads = Roles<kFp8>::kThreads;
+  constexpr int kSmem = smem_bytes<D, kFp8>();
+  auto kern = extend_kernel<D, kFp8>;
+  if (kernel_blocks_per_sm<extend_kernel<D, kFp8>>(kSmem, kThreads) < 0) return SGL_ERR_CUDA;
   const int per_cta = 2 * prm.tpt;
   const unsigned gx = (unsigned)((max_extend + per_cta - 1) / per_cta);
   dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)batch);
-  kern<<<grid, kThreads, smem_bytes<D>(), stream>>>(prm);
+  kern<<<grid, kThreads, kSmem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
 }
 
-template <int D>
+template <int D, bool kFp8>
 sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members,
                       cudaStream_t stream) {
-  auto kern = cascade_group_kernel<D>;
-  if (kernel_blocks_per_sm<cascade_group_kernel<D>>(smem_bytes<D>(), kThreads) < 0)
-    return SGL_ERR_CUDA;
+  constexpr int kThreads = Roles<kFp8>::kThreads;
+  constexpr int kSmem = smem_bytes<D, kFp8>();
+  auto kern = cascade_group_kernel<D, kFp8>;
+  if (kernel_blocks_per_sm<cascade_group_kernel<D, kFp8>>(kSmem, kThreads) < 0) return SGL_ERR_CUDA;
   const int per_cta = 2 * prm.tpt;
   const unsigned gx = (unsigned)((max_members + per_cta - 1) / per_cta);
   dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)n_groups);
-  kern<<<grid, kThreads, smem_bytes<D>(), stream>>>(prm);
+  kern<<<grid, kThreads, kSmem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
+}
+
+template <bool kFp8>
+sgl_status dispatch(int head_dim, bool groups, const Params& prm, int32_t n, int32_t max_rows,
+                    cudaStream_t stream) {
+  if (head_dim == 128)
+    return groups ? run_groups<128, kFp8>(prm, n, max_rows, stream) : run<128, kFp8>(prm, n, max_rows, stream);
+  if (head_dim == 64)
+    return groups ? run_groups<64, kFp8>(prm, n, max_rows, stream) : run<64, kFp8>(prm, n, max_rows, stream);
+  return SGL_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -599,6 +849,8 @@ sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.pool_k = static_cast<const __nv_bfloat16*>(a.pool_k);
   prm.pool_v = static_cast<const __nv_bfloat16*>(a.pool_v);
+  prm.pool_k8 = static_cast<const uint8_t*>(a.pool_k);
+  prm.pool_v8 = static_cast<const uint8_t*>(a.pool_v);
   prm.req_to_token = a.req_to_token;
   prm.rtt_stride = a.rtt_stride;
   prm.req_pool_idx = a.req_pool_idx;
@@ -607,7 +859,11 @@ sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
   prm.g = g;
   prm.tpt = BM / g;
   prm.rows_used = prm.tpt * g;
-  prm.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  // e4m3: scores in units of the widened codes (code * 2^-8) times the K
+  // scale; the states' P.V rows are left in code units (the decode combine
+  // applies the V scale)
+  prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale * kFp8Operand : 1.f);
+  prm.o_scale = a.kv_fp8 ? kFp8Operand : 1.f;
   prm.status = a.status;
   prm.group_start = a.group_start;
   prm.group_len = a.group_len;
@@ -619,9 +875,8 @@ sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
   prm.part_base = a.part_base;
   prm.max_depth = a.max_depth;
   prm.batch = a.batch;
-  if (a.head_dim == 128) return run_groups<128>(prm, a.n_groups, a.max_members, stream);
-  if (a.head_dim == 64) return run_groups<64>(prm, a.n_groups, a.max_members, stream);
-  return SGL_ERR_UNSUPPORTED;
+  return a.kv_fp8 ? dispatch<true>(a.head_dim, true, prm, a.n_groups, a.max_members, stream)
+                  : dispatch<false>(a.head_dim, true, prm, a.n_groups, a.max_members, stream);
 }
 
 size_t extend_workspace_bytes() { return 256; }
@@ -637,6 +892,8 @@ sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream) {
   prm.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
   prm.pool_k = static_cast<const __nv_bfloat16*>(a.pool_k);
   prm.pool_v = static_cast<const __nv_bfloat16*>(a.pool_v);
+  prm.pool_k8 = static_cast<const uint8_t*>(a.pool_k);
+  prm.pool_v8 = static_cast<const uint8_t*>(a.pool_v);
   prm.req_to_token = a.req_to_token;
   prm.rtt_stride = a.rtt_stride;
   prm.req_pool_idx = a.req_pool_idx;
@@ -648,11 +905,13 @@ sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream) {
   prm.g = g;
   prm.tpt = BM / g;
   prm.rows_used = prm.tpt * g;
-  prm.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  // e4m3: scores in units of the widened codes (code * 2^-8) times the K
+  // scale; the output takes the V scale and the 2^8 back
+  prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale * kFp8Operand : 1.f);
+  prm.o_scale = a.kv_fp8 ? a.v_scale * kFp8Operand : 1.f;
   prm.status = static_cast<int*>(a.workspace);
-  if (a.head_dim == 128) return run<128>(prm, a.batch, a.max_extend, stream);
-  if (a.head_dim == 64) return run<64>(prm, a.batch, a.max_extend, stream);
-  return SGL_ERR_UNSUPPORTED;
+  return a.kv_fp8 ? dispatch<true>(a.head_dim, false, prm, a.batch, a.max_extend, stream)
+                  : dispatch<false>(a.head_dim, false, prm, a.batch, a.max_extend, stream);
 }
 
 }  // namespace sgl

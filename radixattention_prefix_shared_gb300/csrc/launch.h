@@ -102,6 +102,10 @@ struct GroupArgs {
   int* status;
   int32_t num_q_heads, num_kv_heads, head_dim;
   float sm_scale;
+  // e4m3 pool: the K scale folds into the scores; the states' P.V rows stay
+  // in code units
+  bool kv_fp8 = false;
+  float k_scale = 1.f;
 };
 sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream);
 
@@ -122,6 +126,10 @@ struct ExtendArgs {
   void* workspace;
   int32_t num_q_heads, num_kv_heads, head_dim;
   float sm_scale;
+  // e4m3 pool (kv_fp8): every key and value, the suffix's included, is read
+  // from the pool through req_to_token; k_new / v_new are unused
+  bool kv_fp8 = false;
+  float k_scale = 1.f, v_scale = 1.f;
 };
 size_t extend_workspace_bytes();
 sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream);
