@@ -297,6 +297,12 @@ SGL_DEV uint32_t e4m3x2_to_f16x2(uint32_t two) {
 template <int D, int G, int LPT>
 __host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
 
+// e4m3 operands of the tensor-core path: 1 = widened by bit placement on the
+// integer pipe (code * 2^-8 as f16, the 2^8 folded back into the scores and
+// the published sums), 0 = the hardware e4m3x2 -> f16x2 conversion
+#ifndef SGL_DECODE_FP8_WIDEN
+#define SGL_DECODE_FP8_WIDEN 1
+#endif
 #ifndef SGL_DECODE_MMA
 #define SGL_DECODE_MMA 2
 #endif
@@ -537,7 +543,18 @@ struct MmaState {
           : "r"(qa[ks_][0]), "r"(a1), "r"(qa[ks_][1]), "r"(a3), "r"(b0), "r"(b1));
     }
   }
-  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2) {
+  // widened e4m3 operands hold code * 2^-8 (bit placement) or code (cvt)
+  static constexpr float kWiden = (kBytes == 1 && SGL_DECODE_FP8_WIDEN) ? 256.f : 1.f;
+  SGL_DEV static void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if constexpr (SGL_DECODE_FP8_WIDEN) {
+      e4m3x4_to_f16x2_scaled(w, lo, hi);
+    } else {
+      lo = e4m3x2_to_f16x2(w);
+      hi = e4m3x2_to_f16x2(w >> 16);
+    }
+  }
+  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2_in) {
+    const float scale_log2 = scale_log2_in * kWiden;
     // ---- S = q.k for this warp's KW keys, 8 at a time; sv[nb][row set][c]
     float sv[KW / 8][NR][2];
 #pragma unroll
@@ -557,8 +574,11 @@ struct MmaState {
           const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            qk(d4, 4 * v + i, e4m3x2_to_f16x2(ws[i]), e4m3x2_to_f16x2(ws[i] >> 16));
+          for (int i = 0; i < 4; ++i) {
+            uint32_t lo, hi;
+            widen4(ws[i], lo, hi);
+            qk(d4, 4 * v + i, lo, hi);
+          }
         }
       }
 #pragma unroll
@@ -629,10 +649,11 @@ struct MmaState {
         const uint32_t y1 = *reinterpret_cast<const uint32_t*>(r0 + 9 * kRowBytes + col);
         const uint32_t xa = __byte_perm(x0, x1, 0x5140), xb = __byte_perm(x0, x1, 0x7362);
         const uint32_t ya = __byte_perm(y0, y1, 0x5140), yb = __byte_perm(y0, y1, 0x7362);
-        const uint32_t b0[4] = {e4m3x2_to_f16x2(xa), e4m3x2_to_f16x2(xa >> 16), e4m3x2_to_f16x2(xb),
-                                e4m3x2_to_f16x2(xb >> 16)};
-        const uint32_t b1[4] = {e4m3x2_to_f16x2(ya), e4m3x2_to_f16x2(ya >> 16), e4m3x2_to_f16x2(yb),
-                                e4m3x2_to_f16x2(yb >> 16)};
+        uint32_t b0[4], b1[4];
+        widen4(xa, b0[0], b0[1]);
+        widen4(xb, b0[2], b0[3]);
+        widen4(ya, b1[0], b1[1]);
+        widen4(yb, b1[2], b1[3]);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           asm volatile(
@@ -656,8 +677,8 @@ struct MmaState {
         for (int b = 0; b < SB; ++b)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            dst[32 * b + j] = o[b][j][2 * rr];
-            dst[32 * b + 4 + j] = o[b][j][2 * rr + 1];
+            dst[32 * b + j] = o[b][j][2 * rr] * kWiden;  // back to code units
+            dst[32 * b + 4 + j] = o[b][j][2 * rr + 1] * kWiden;
           }
         if (t == 0) {
           red_m[warp * G + row] = m[rr];
