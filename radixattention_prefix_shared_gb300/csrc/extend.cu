@@ -707,7 +707,12 @@ SGL_DEV void attend_tiles(const Params& p) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idS = make_idesc_bf16(BM, BN, false, kFp8);
     constexpr uint32_t idO = make_idesc_bf16(BM, D, true, kFp8);
+    // The issuing thread is the critical path: the tensor pipe idles while it
+    // waits, so it polls with short probes first (it resumes as soon as the
+    // phase completes) before the bounded wait.
     auto wait = [&](uint64_t* bar, uint32_t parity) {
+      for (int i = 0; i < 64; ++i)
+        if (mbar_try_wait(bar, parity, 200u)) return true;
       return mbar_wait_bounded(bar, parity, &bars->abort, p.status);
     };
     auto issue_s = [&](int t, int stage) {
@@ -735,18 +740,20 @@ SGL_DEV void attend_tiles(const Params& p) {
       tc_fence_after();
     }
     for (int b = 0; b < nb && ok; ++b) {
+      // V of the previous block, K of this one and P of tile 0, then one
+      // proxy fence for both landed tiles
       const int kt = 2 * b, ks = kt % C::kStages;
-      if (!(ok = wait(&bars->kv_full[ks], (kt / C::kStages) & 1))) break;
-      fence_proxy_async_smem();
-      tc_fence_after();
       int vt = 0, vs = 0;
       if (b > 0) {
         vt = 2 * b - 1;
         vs = vt % C::kStages;
-        if (!(ok = wait(&bars->p_ready[0], (b - 1) & 1))) break;
         if (!(ok = wait(&bars->kv_full[vs], (vt / C::kStages) & 1))) break;
-        fence_proxy_async_smem();
-        tc_fence_after();
+      }
+      if (!(ok = wait(&bars->kv_full[ks], (kt / C::kStages) & 1))) break;
+      if (b > 0 && !(ok = wait(&bars->p_ready[0], (b - 1) & 1))) break;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      if (b > 0) {
         issue_pv(0, vs, b > 1);
       }
       issue_s(0, ks);
