@@ -39,9 +39,11 @@
 // correction pass.
 //
 // e4m3 pool: every key and value -- the suffix too, stored before the call --
-// is gathered through req_to_token as codes.  Four producer warps (one per
-// SM sub-partition) stage the codes with cp.async and widen them to f16 into
-// the swizzled ring with integer ops: the code's seven magnitude bits placed
+// is gathered through req_to_token as codes.  Three producer warps stage the
+// codes with cp.async and widen them to f16 into the swizzled ring with
+// integer ops, and the softmax runs as 8 warps that own whole rows (one
+// thread a row, all 128 keys of a block; no pair vote), so each producer
+// shares its sub-partition with two softmax warps instead of four: the code's seven magnitude bits placed
 // at f16 bit 7 (sign at bit 15) read as exactly code * 2^-8, subnormal codes
 // included, so both MMAs run on f16 operands (the query is widened from bf16,
 // P is packed as f16 with the lazy bound lowered to 2^15) and the 2^8 and the
@@ -59,7 +61,15 @@ namespace {
 
 constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per KV block
-constexpr int kSoftmaxWarps = 16;
+// softmax layout per pool type (measured: whole rows equal on bf16 pools,
+// +10% on e4m3 pools, whose producers then share each sub-partition with two
+// softmax warps instead of four)
+#ifndef SGL_EXTEND_FULL_ROWS_BF16
+#define SGL_EXTEND_FULL_ROWS_BF16 0
+#endif
+#ifndef SGL_EXTEND_FULL_ROWS_FP8
+#define SGL_EXTEND_FULL_ROWS_FP8 1
+#endif
 constexpr uint32_t kTmemCols = 512;
 // e4m3 codes widened by bit placement hold code * 2^-8
 constexpr float kFp8Operand = 256.0f;
@@ -77,13 +87,17 @@ constexpr float kFp8Operand = 256.0f;
 #endif
 
 // warp roles: softmax warps, producer warps, the MMA warp
-// (e4m3: three producer warps, on sub-partitions 0-2 with the MMA warp on
-// the fourth; 20 warps leave 96 registers a thread, 21 would leave 80)
+// (e4m3: three producer warps; with whole-row softmax 12 warps leave 168
+// registers a thread)
 template <bool kFp8>
 struct Roles {
+  // softmax: 8 warps owning whole rows (one thread a row, all 128 keys of a
+  // block), or 16 warps in pairs splitting each row's keys
+  static constexpr bool kFullRows = kFp8 ? SGL_EXTEND_FULL_ROWS_FP8 : SGL_EXTEND_FULL_ROWS_BF16;
+  static constexpr int kSoftmaxWarps = kFullRows ? 8 : 16;
   static constexpr int kProducerWarps = kFp8 ? 3 : 2;
-  static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;  // 18 (bf16), 19 (e4m3)
-  static constexpr int kThreads = (kMmaWarp + 1) * 32;              // 608, 640
+  static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
+  static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kProducerThreads = kProducerWarps * 32;
   // a producer thread copies 16-byte chunk (ptid % 8) of the bf16 rows
   // ptid / 8 + kRowStep * i < 128, i < kRowsPerThread, of every 128-row tile
@@ -416,7 +430,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     mbar_init(&bars->q_full, R::kProducerThreads);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_ready[t], 8 * 32);  // the 8 softmax warps of the tile
+      mbar_init(&bars->p_ready[t], R::kSoftmaxWarps / 2 * 32);  // the softmax warps of the tile
     }
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
@@ -442,7 +456,162 @@ SGL_DEV void attend_tiles(const Params& p) {
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
 
-  if (warp < kSoftmaxWarps) {
+  if (R::kFullRows && warp < R::kSoftmaxWarps) {
+    if constexpr (R::kFullRows) {
+    // ------------------------------------------------------------ softmax (whole rows)
+    // warp w: Q tile t = w / 4, TMEM lane quarter q = w % 4 (rows 32q..);
+    // every thread owns one row: all 128 keys of a block, all D columns of O.
+    // A row whose block sum breaks the bound moves its own reference (the
+    // warp reloads S and rescales O together, rows keeping their reference
+    // recompute the same P with alpha = 1), so no two warps ever agree on
+    // anything.
+    const int t = warp >> 2, q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t tS = tmem + lane_off + col_s(t);
+    const uint32_t tO = tmem + lane_off + col_o(t);
+    const int tok = q0 + t * p.tpt + row / p.g;
+    const bool row_valid = row < p.rows_used && tok < e;
+    const int tok_i = row_valid ? tok : (1 << 30);  // padding rows see every key
+    const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int b = 0; b < nb; ++b) {
+      if (!warp_wait(&bars->s_full[t], b & 1, bars, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // visible keys of this block: c < limit (key index within the block)
+      int limit;
+      if (b < nb_pre) limit = pfx - b * BN;
+      else limit = tok_i - (b - nb_pre) * BN + 1;
+      limit = max(0, min(BN, limit));
+      uint32_t sr[BN];
+      auto load_s = [&]() {
+#pragma unroll
+        for (int j = 0; j < BN / 32; ++j)
+          tmem_ld32(tS + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * j]));
+        tmem_wait_ld();
+        if (limit < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= limit) sr[c] = __float_as_uint(-INFINITY);
+        }
+      };
+      // P of the row's 128 keys against reference m_use, packed in place
+      // over sr[0..63]; returns the row sum
+      auto make_p = [&](float m_use) {
+        const float2 nm = make_float2(-m_use, -m_use);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          const float2 x =
+              ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc, nm);
+          float2 pw;
+          if ((c & 7) >= 8 - kFmaExpPairsPer8) {
+            pw = exp2_fma2(x);
+          } else {
+            pw = make_float2(ex2(x.x), ex2(x.y));
+          }
+          if (c & 1) acc1 = fadd2(acc1, pw);
+          else acc0 = fadd2(acc0, pw);
+          sr[c] = kFp8 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
+        }
+        return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      };
+      load_s();
+      float psum = 0.f, alpha = 1.f;
+      bool need = b == 0;
+      if (b > 0) {
+        // lazy reference: accept the block while the row sum stays within
+        // the bound (every weight then fits the P operand type)
+        psum = make_p(m_ref);
+        need = !(psum <= R::kAcceptSum);
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        if (b > 0) load_s();  // P overwrote the registers; S is still in TMEM
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < BN; c += 2)
+          mq[(c >> 1) & 3] = fmax3(mq[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
+        const float m_new = need ? fmaxf(m_ref, mx) : m_ref;
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+        m_ref = m_new;
+        psum = make_p(m_ref == -INFINITY ? 0.f : m_ref);
+        if (b > 0) {
+          // O holds blocks < b: bring it to the row's reference (alpha = 1
+          // for rows that kept theirs)
+#pragma unroll
+          for (int j = 0; j < D / 32; ++j) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * j, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + 32 * j, o);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j)
+        tmem_st32(tS + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * j]));
+      l = l * alpha + psum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready[t]);
+    }
+    if (ok) ok = warp_wait(&bars->o_done, 0, bars, p.status);
+    if (ok) {
+      tc_fence_after();
+      if constexpr (kGroup) {
+        const int rm = row_valid ? p.members[mbeg + tok] : 0;
+        const int dep = p.group_depth[r];
+        const bool wr = row_valid && rm >= 0 && rm < p.batch && dep >= 0 && dep < p.max_depth;
+        const int64_t ent =
+            ((p.part_base + (int64_t)rm * p.max_depth + dep) * p.Hkv + kvh) * p.g + row % p.g;
+        float* dst = p.part_acc + ent * D;
+        const float os = kFp8 ? p.o_scale : 1.f;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * j, o);
+          tmem_wait_ld();
+          if (wr) {
+            float4* d4 = reinterpret_cast<float4*>(dst + 32 * j);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              d4[v] = make_float4(__uint_as_float(o[4 * v]) * os, __uint_as_float(o[4 * v + 1]) * os,
+                                  __uint_as_float(o[4 * v + 2]) * os, __uint_as_float(o[4 * v + 3]) * os);
+          }
+        }
+        if (wr) p.part_ml[ent] = make_float2(m_ref, l);
+      } else {
+        const float inv = l > 0.f ? (kFp8 ? p.o_scale : 1.f) / l : 0.f;
+        __nv_bfloat16* orow =
+            p.out + ((int64_t)(off + tok) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * j, o);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * j);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+      }
+    }
+    }
+  } else if (warp < R::kSoftmaxWarps) {
+    if constexpr (!R::kFullRows) {
     // ------------------------------------------------------------ softmax
     // warp w: Q tile t, key-column half h, TMEM lane quarter q (rows 32q..)
     const int t = (warp >> 2) & 1, h = warp >> 3, q = warp & 3;
@@ -612,14 +781,15 @@ SGL_DEV void attend_tiles(const Params& p) {
         }
       }
     }
+    }
   } else if (warp < R::kMmaWarp) {
     // ------------------------------------------------------------ producers
     if constexpr (kFp8) {
-      produce_fp8<D, kGroup>(p, sQ_a, sKV, sRaw, bars, tid - kSoftmaxWarps * 32, e, mbeg, q0, pfx,
+      produce_fp8<D, kGroup>(p, sQ_a, sKV, sRaw, bars, tid - R::kSoftmaxWarps * 32, e, mbeg, q0, pfx,
                              q_end, nb_pre, nb, off);
     } else {
     constexpr int kRowStep = R::kRowStep, kRowsPerThread = R::kRowsPerThread;
-    const int ptid = tid - kSoftmaxWarps * 32;
+    const int ptid = tid - R::kSoftmaxWarps * 32;
     const int ci = ptid & 7;
     const int rbase = ptid >> 3;  // rows rbase + kRowStep * i
     // Q tiles
