@@ -168,6 +168,44 @@ def test_fp8_validation(cuda_lib):
              ctypes.byref(d), None) == 0
 
 
+def test_fp8_extend_and_cascade_validation(cuda_lib):
+    """The e4m3 extend takes no k_new / v_new (the suffix is read from the
+    pool) and rejects bad scales; the e4m3 cascade validates like the bf16 one."""
+    d = _dims()
+    x = cuda_lib.sgl_extend_attention_fp8
+
+    def ext(**kw):
+        a = dict(q=FAKE, pk=FAKE, pv=FAKE, ks=1.0, vs=1.0, rtt=FAKE, rows=4, stride=64, rpi=FAKE,
+                 pl=FAKE, el=FAKE, batch=2, total=10, max_e=6, max_p=30, out=FAKE, ws=FAKE, wsb=256)
+        a.update(kw)
+        return x(a["q"], a["pk"], a["pv"], a["ks"], a["vs"], a["rtt"], a["rows"], a["stride"], a["rpi"],
+                 a["pl"], a["el"], a["batch"], a["total"], a["max_e"], a["max_p"], a["out"], a["ws"],
+                 a["wsb"], ctypes.byref(d), None)
+    assert ext(ks=0.0) == 1 and ext(vs=float("nan")) == 1 and ext(ks=float("inf")) == 1
+    assert ext(batch=0) == 0
+    assert ext(q=None) == 1 and ext(pk=MISALIGNED) == 1 and ext(out=MISALIGNED) == 1
+    assert ext(max_e=11) == 1
+    assert ext(ws=None) == 3 and ext(wsb=16) == 3
+    dd = _dims(head_dim=96)
+    assert x(FAKE, FAKE, FAKE, 1.0, 1.0, FAKE, 4, 64, FAKE, FAKE, FAKE, 2, 10, 6, 30, FAKE, FAKE, 256,
+             ctypes.byref(dd), None) == 2
+    c = cuda_lib.sgl_cascade_decode_attention_fp8
+    dc = _dims(num_q_heads=16, num_kv_heads=4)
+    need = B.cascade_decode_workspace_bytes(8, 512, 3, dc)
+
+    def casc(**kw):
+        a = dict(ks=1.0, vs=1.0, q=FAKE, gs=FAKE, n_groups=2, max_d=3, ws=FAKE, wsb=need)
+        a.update(kw)
+        return c(a["q"], FAKE, FAKE, a["ks"], a["vs"], FAKE, 8, 512, FAKE, FAKE, 8, 512, a["gs"], FAKE, FAKE,
+                 FAKE, FAKE, a["n_groups"], 4, a["max_d"], FAKE, a["ws"], a["wsb"], ctypes.byref(dc), None)
+    assert casc(ks=-1.0) == 1 and casc(vs=0.0) == 1
+    assert casc(gs=None) == 1 and casc(max_d=0) == 1 and casc(q=MISALIGNED) == 1
+    assert casc(ws=None) == 3 and casc(wsb=need - 1) == 3
+    ch = cuda_lib.sgl_check_extend_fp8_indices
+    assert ch(FAKE, 0, 64, FAKE, FAKE, FAKE, 2, 10, 6, 30, 1024, FAKE, None) == 1
+    assert ch(FAKE, 4, 64, FAKE, FAKE, FAKE, 0, 0, 0, 0, 1024, FAKE, None) == 0
+
+
 def test_check_calls_validate_on_host(cuda_lib):
     assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, None, None) == 1
     assert cuda_lib.sgl_check_store_kv_indices(FAKE, 4, 1024, FAKE, 16, FAKE, None) == 3  # bitmap small
