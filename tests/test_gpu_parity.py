@@ -71,6 +71,8 @@ EXTEND_SHAPES = [
     (16, 2, 64, [40, 0, 700], [9, 100, 31]),
     (8, 1, 128, [129], [40]),
     (6, 2, 128, [70, 3], [50, 90]),          # g = 3: 42 tokens per tile, 2 padding rows
+    (16, 1, 128, [100, 0], [40, 17]),        # g = 16: 8 tokens per tile
+    (32, 1, 64, [64, 7], [33, 20]),          # g = 32: 4 tokens per tile
 ]
 
 
@@ -115,6 +117,23 @@ def test_decode_matches_oracle(shape):
     w = decode_case(sum(S), Hq=Hq, Hkv=Hkv, D=D, seq_lens=S)
     got = Run(w).decode()
     assert_close(got, oracle_decode(w), f"decode {shape}")
+
+
+def test_decode_long_context():
+    """128 K-token and 70 K-token rows: 128 and 69 splits of at most 1,024 keys
+    merged by the combine; a 3-key row beside them."""
+    w = decode_case(77, Hq=8, Hkv=2, D=128, seq_lens=[131072, 70001, 3])
+    got = Run(w).decode()
+    assert_close(got, oracle_decode(w, pool=w.pool_view(decode_steps=1)), "decode 128K context")
+
+
+def test_extend_long_prefix_sampled():
+    """A 64 K-token cached prefix (512 key blocks before the suffix), sampled rows."""
+    w = extend_case(78, Hq=8, Hkv=2, D=128, prefix_lens=[65536, 1000], extend_lens=[300, 129])
+    got = Run(w).extend()
+    toks = [0, 1, 150, 299, 300, 428]
+    assert_close(got[toks], oracle_extend(w, tokens=toks, pool=w.pool_view(with_extend=False)),
+                 "extend 64K prefix")
 
 
 def test_single_key_outputs_are_bit_exact():
