@@ -690,7 +690,12 @@ struct MmaState {
 };
 
 template <int D, int G, int LPT, typename KV>
-__host__ __device__ constexpr int split_min_blocks() { return use_mma<KV, G>() ? 3 : min_blocks<D, G, LPT>(); }
+#ifndef SGL_DECODE_MMA_MIN_BLOCKS
+#define SGL_DECODE_MMA_MIN_BLOCKS 3
+#endif
+__host__ __device__ constexpr int split_min_blocks() {
+  return use_mma<KV, G>() ? SGL_DECODE_MMA_MIN_BLOCKS : min_blocks<D, G, LPT>();
+}
 
 // Ring shape of the split kernel: the tensor-core path takes 32 bf16 keys per
 // stage (8 per warp), the CUDA-core path its own tile and depth.  A stage
