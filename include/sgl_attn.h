@@ -23,7 +23,7 @@
  *     are not read on the host.  Out-of-range values are undefined behaviour in
  *     the fast path; the sgl_check_* calls detect them without trapping.
  *   - head_dim must be 64 or 128; num_q_heads must be a multiple of
- *     num_kv_heads; decode is built for 1..8 or 16 query heads per KV head
+ *     num_kv_heads; decode is built for 1..16 query heads per KV head
  *     (extend for up to 128).  Violations return SGL_ERR_UNSUPPORTED or
  *     SGL_ERR_INVALID_ARG before anything is launched.
  */

@@ -908,6 +908,13 @@ sgl_status run_g(int G, const Params& prm, int64_t max_items, const Groups& gr,
     case 5: return run<D, 5, KV>(prm, max_items, gr, ga, stream);
     case 6: return run<D, 6, KV>(prm, max_items, gr, ga, stream);
     case 7: return run<D, 7, KV>(prm, max_items, gr, ga, stream);
+    case 9: return run<D, 9, KV>(prm, max_items, gr, ga, stream);
+    case 10: return run<D, 10, KV>(prm, max_items, gr, ga, stream);
+    case 11: return run<D, 11, KV>(prm, max_items, gr, ga, stream);
+    case 12: return run<D, 12, KV>(prm, max_items, gr, ga, stream);
+    case 13: return run<D, 13, KV>(prm, max_items, gr, ga, stream);
+    case 14: return run<D, 14, KV>(prm, max_items, gr, ga, stream);
+    case 15: return run<D, 15, KV>(prm, max_items, gr, ga, stream);
     case 16: return run<D, 16, KV>(prm, max_items, gr, ga, stream);
     default: return SGL_ERR_UNSUPPORTED;
   }
@@ -926,7 +933,7 @@ size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, in
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.batch == 0) return SGL_OK;
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (!((G >= 1 && G <= 8) || G == 16)) return SGL_ERR_UNSUPPORTED;
+  if (G < 1 || G > 16) return SGL_ERR_UNSUPPORTED;
   const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);

@@ -56,6 +56,7 @@ TREES = [
     (4, 2, 64, (2, 2, 2), (120, 140), (0, 1)),      # g = 2, D = 64
     (12, 2, 128, (2, 3), (40, 300), (0, 50)),        # g = 6
     (32, 2, 128, (3, 2), (10, 200), (1, 30)),        # g = 16
+    (24, 2, 128, (2, 3), (20, 150), (0, 20)),        # g = 12
 ]
 
 

@@ -108,6 +108,11 @@ DECODE_SHAPES = [
     (28, 4, 128, [1025, 64]),
     (32, 2, 128, [900, 1, 4100]),
     (16, 1, 64, [513]),
+    # group sizes 9..15: rows 8..15 partly filled
+    (18, 2, 128, [700, 33]),
+    (24, 2, 64, [1500, 1]),
+    (30, 2, 128, [513, 2049]),
+    (13, 1, 128, [800]),
 ]
 
 
