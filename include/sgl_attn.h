@@ -23,8 +23,9 @@
  *     are not read on the host.  Out-of-range values are undefined behaviour in
  *     the fast path; the sgl_check_* calls detect them without trapping.
  *   - head_dim must be 64 or 128; num_q_heads must be a multiple of
- *     num_kv_heads; decode is built for 1..16 query heads per KV head
- *     (extend for up to 128).  Violations return SGL_ERR_UNSUPPORTED or
+ *     num_kv_heads, with up to 128 query heads per KV head (decode runs a
+ *     group of more than 16 as KV-head copies of at most 16 query heads
+ *     each, every copy reading the KV head's rows).  Violations return SGL_ERR_UNSUPPORTED or
  *     SGL_ERR_INVALID_ARG before anything is launched.
  */
 #ifndef SGL_ATTN_H

@@ -136,7 +136,13 @@ struct Params {
   const int32_t* req_pool_idx;
   const int32_t* seq_lens;
   __nv_bfloat16* out;
+  // Hkv: KV heads as the kernels see them.  A group of more than 16 query
+  // heads per KV head runs as kv_split "virtual" KV heads of Hq / Hkv query
+  // heads each (virtual head v reads pool head v / kv_split; query heads,
+  // outputs and partial states keep the same flat order); Hkv_pool is the
+  // pool's own KV head count (the row stride of a slot).
   int32_t batch, Hq, Hkv;
+  int32_t kv_split, Hkv_pool;
   float scale_log2;  // softmax scale * log2(e) * K scale (1 for a bf16 pool)
   float v_scale;     // V scale of an e4m3 pool (1 for bf16), applied to the output
   Ws ws;
@@ -757,8 +763,8 @@ decode_split_kernel(Params p) {
     __syncthreads();  // slots visible; previous item's reduction scratch free
 
     const int n_tiles = (n + kTile - 1) / kTile;
-    const uint8_t* kbase = p.pool_k + (int64_t)kvh * L::kRowBytes;
-    const uint8_t* vbase = p.pool_v + (int64_t)kvh * L::kRowBytes;
+    const uint8_t* kbase = p.pool_k + (int64_t)(kvh / p.kv_split) * L::kRowBytes;
+    const uint8_t* vbase = p.pool_v + (int64_t)(kvh / p.kv_split) * L::kRowBytes;
     auto issue = [&](int tile, int stage) {
       const uint32_t st_a = ring + stage * kStageBytes;
       constexpr int kRowsPerPass = kThreads / L::kRowVecs;
@@ -768,7 +774,7 @@ decode_split_kernel(Params p) {
         const int tok = pass * kRowsPerPass + tid / L::kRowVecs;
         const int32_t j = tile * kTile + tok;
         const bool ok = j < n;
-        const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv : 0;
+        const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv_pool : 0;
         const uint32_t d = st_a + tok * L::kRowBytes + vec * 16;
         cp_async_16(d, kbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
         cp_async_16(d + kTileBytes, vbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
@@ -922,18 +928,32 @@ sgl_status run_g(int G, const Params& prm, int64_t max_items, const Groups& gr,
 
 }  // namespace
 
+// Split factor for groups of more than 16 query heads per KV head: the
+// smallest s dividing G with G / s <= 16 (1 for G <= 16).
+static int32_t kv_split_for(int32_t G) {
+  if (G <= 16) return 1;
+  for (int32_t s = 2; s <= G; ++s)
+    if (G % s == 0 && G / s <= 16) return s;
+  return G;
+}
+
 size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, int32_t Hkv,
                               int32_t D, bool cascade, int32_t max_depth) {
   const size_t head = cascade ? kCascadeStatusBytes : 0;
-  if (batch <= 0 || max_seq_len <= 0 || Hkv <= 0) return head + 256;
-  return head + ws_layout(batch, max_items_for(batch, max_seq_len), Hkv, Hq / Hkv, D,
+  if (batch <= 0 || max_seq_len <= 0 || Hkv <= 0 || Hq < Hkv) return head + 256;
+  const int32_t split = kv_split_for(Hq / Hkv);
+  return head + ws_layout(batch, max_items_for(batch, max_seq_len), Hkv * split, Hq / Hkv / split, D,
                           cascade ? max_depth : 0, cascade, nullptr, nullptr);
 }
 
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.batch == 0) return SGL_OK;
-  const int G = a.num_q_heads / a.num_kv_heads;
-  if (G < 1 || G > 16) return SGL_ERR_UNSUPPORTED;
+  const int G_pool = a.num_q_heads / a.num_kv_heads;
+  if (G_pool < 1 || G_pool > 128) return SGL_ERR_UNSUPPORTED;
+  const int split = kv_split_for(G_pool);
+  const int G = G_pool / split;                 // query heads of a (virtual) KV head
+  const int Hkv = a.num_kv_heads * split;       // KV heads as the kernels see them
+  if (Hkv > 65535) return SGL_ERR_UNSUPPORTED;  // grid y
   const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -946,7 +966,9 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.out = static_cast<__nv_bfloat16*>(a.out);
   prm.batch = a.batch;
   prm.Hq = a.num_q_heads;
-  prm.Hkv = a.num_kv_heads;
+  prm.Hkv = Hkv;
+  prm.kv_split = split;
+  prm.Hkv_pool = a.num_kv_heads;
   // the K scale of an e4m3 pool folds into the query, the V scale into the output
   prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale : 1.f);
   prm.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
@@ -956,7 +978,7 @@ sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int32_t max_depth = a.cascade ? a.max_depth : 0;
   char* base = static_cast<char*>(a.workspace);
   if (base == nullptr) return SGL_ERR_WORKSPACE;
-  const size_t need = head + ws_layout(a.batch, max_items, a.num_kv_heads, G, a.head_dim, max_depth,
+  const size_t need = head + ws_layout(a.batch, max_items, Hkv, G, a.head_dim, max_depth,
                                        a.cascade, base + head, &prm.ws);
   if (a.workspace_bytes < need) return SGL_ERR_WORKSPACE;
   prm.group_base = max_items;

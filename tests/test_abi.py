@@ -108,10 +108,13 @@ def test_decode_validation_and_workspace_size(cuda_lib):
     assert call(sl=None) == 1
     assert call(ws=None) == 3
     assert call(wsb=B.decode_workspace_bytes(2, 64, d) - 1) == 3
-    # query heads per KV head: 1..16 are built
-    d17 = _dims(num_q_heads=34, num_kv_heads=2)
+    # query heads per KV head: up to 128
+    d129 = _dims(num_q_heads=258, num_kv_heads=2)
     assert f(FAKE, FAKE, FAKE, FAKE, 4, 64, FAKE, FAKE, 2, 64, FAKE, FAKE,
-             B.decode_workspace_bytes(2, 64, d17), ctypes.byref(d17), None) == 2
+             B.decode_workspace_bytes(2, 64, d129), ctypes.byref(d129), None) == 2
+    # groups above 16 run as KV-head copies: the scratch is the same size per query head
+    assert B.decode_workspace_bytes(2, 64, _dims(num_q_heads=64, num_kv_heads=2)) >= \
+        B.decode_workspace_bytes(2, 64, _dims(num_q_heads=32, num_kv_heads=2))
     assert B.extend_workspace_bytes(8, 16384, d) >= 16
 
 

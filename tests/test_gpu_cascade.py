@@ -57,6 +57,7 @@ TREES = [
     (12, 2, 128, (2, 3), (40, 300), (0, 50)),        # g = 6
     (32, 2, 128, (3, 2), (10, 200), (1, 30)),        # g = 16
     (24, 2, 128, (2, 3), (20, 150), (0, 20)),        # g = 12
+    (32, 1, 128, (2, 3), (20, 150), (0, 20)),        # g = 32: two KV-head copies in decode
 ]
 
 

@@ -113,6 +113,10 @@ DECODE_SHAPES = [
     (24, 2, 64, [1500, 1]),
     (30, 2, 128, [513, 2049]),
     (13, 1, 128, [800]),
+    # groups above 16: KV-head copies of <= 16 query heads
+    (32, 1, 128, [900, 33]),                 # 2 x 16
+    (48, 2, 128, [700, 2]),                  # 2 x 12 per KV head
+    (34, 2, 64, [500, 1]),                   # 17 = 17 x 1 (prime)
 ]
 
 
