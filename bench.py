@@ -379,8 +379,14 @@ SMALL = {2: dict(pool_size=1 << 18), 3: dict(pool_size=1 << 17),
          4: dict(pool_size=1 << 18), 5: dict(pool_size=1 << 19, n_decode=24)}
 
 
+PAGED = (2, 3)  # workloads that lay their slots out in whole pages when asked
+
+
 def small_kwargs(args):
-    return SMALL.get(args.config, {}) if getattr(args, "small", False) else {}
+    kw = dict(SMALL.get(args.config, {})) if getattr(args, "small", False) else {}
+    if getattr(args, "page_size", 1) > 1:
+        kw["page_size"] = args.page_size
+    return kw
 
 
 def prefix_sharing(rows):
@@ -610,6 +616,7 @@ def gpu_arm(args):
                    "launch": "cuda_graph" if graph is not None else "eager",
                    "extend_decode_overlap": step.overlap,
                    "kv_cache_dtype": "fp8_e4m3" if step.fp8 else "bf16",
+                   "page_size": int(w.recipe.get("page_size", 1)),
                    "prefix_sharing": sharing_of(w),
                    "l2": "flushed between steps (256 MiB write)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_bytes),
@@ -743,9 +750,13 @@ def main(argv=None):
                     help="decode through shared-prefix groups (auto: when the batch shares prefixes)")
     ap.add_argument("--small", action="store_true",
                     help="reduced pool / batch of the workload, for profiler captures")
+    ap.add_argument("--page-size", type=int, default=1,
+                    help="requests own whole pages of this many consecutive slots (configs 2 and 3)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.page_size < 1 or (args.page_size > 1 and args.config not in PAGED):
+        ap.error(f"--page-size > 1 is built for configs {PAGED}")
     if args.impl == "reference":
         reference_arm(args)
     else:

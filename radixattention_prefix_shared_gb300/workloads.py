@@ -518,40 +518,73 @@ def tiny(seed: int = 1001) -> Workload:
     return w
 
 
+def _page_runs(g: np.random.Generator, pool_size: int, page_size: int, lens) -> list:
+    """Slots of requests that own whole pages: pages of ``page_size``
+    consecutive slots are taken from one seeded permutation of the pool's
+    pages, ceil(n / page_size) per request, and request j's positions fill its
+    pages in order (the tail of its last page stays free)."""
+    pages = g.permutation(pool_size // page_size).astype(np.int64)
+    out, pos = [], 0
+    for n in lens:
+        k = -(-int(n) // page_size)
+        mine = pages[pos: pos + k]
+        pos += k
+        assert mine.size == k, "pool too small"
+        out.append((mine[:, None] * page_size + np.arange(page_size)).reshape(-1)[: int(n)].astype(np.int32))
+    return out
+
+
 def decode_llama7b(seed: int = 1002, batch: int = 64, pool_size: int = 1 << 20,
-                   seq_range=(512, 4096)) -> Workload:
+                   seq_range=(512, 4096), page_size: int = 1) -> Workload:
     """Plain paged decode, Llama-7B-like heads (32 q / 32 kv, head_dim 128).
 
     seq_lens ~ U[512, 4096] (integers, inclusive) including the new token; every
     token's slot is drawn without replacement from one seeded permutation of
     the pool (fully fragmented); the new token's slot is the last of its row.
+    With ``page_size`` > 1 every request owns whole pages of that many
+    consecutive slots instead (``_page_runs``), its new token in them.
     """
     dims = Dims(32, 32, 128, pool_size, 1.0 / math.sqrt(128))
     g = _rng(seed, _S_LAYOUT + 100)
     seq = g.integers(seq_range[0], seq_range[1] + 1, size=batch).astype(np.int32)
+    recipe = dict(batch=batch, seq_range=list(seq_range), pool=pool_size, page_size=page_size)
+    if page_size > 1:
+        rows = _page_runs(g, pool_size, page_size, seq)
+        return build_workload("decode_llama7b", dims, seed, decode_ctx=[r[:-1] for r in rows], std=1.0,
+                              rtt_stride=int(seq_range[1]),
+                              slot_source=np.array([r[-1] for r in rows], np.int32), recipe=recipe)
     perm = g.permutation(pool_size).astype(np.int32)
     ctx, pos = [], 0
     for s in seq:
         ctx.append(perm[pos: pos + s - 1])
         pos += s - 1
     return build_workload("decode_llama7b", dims, seed, decode_ctx=ctx, std=1.0,
-                          rtt_stride=int(seq_range[1]), slot_source=perm[pos:],
-                          recipe=dict(batch=batch, seq_range=list(seq_range), pool=pool_size))
+                          rtt_stride=int(seq_range[1]), slot_source=perm[pos:], recipe=recipe)
 
 
 def shared_prompt_extend(seed: int = 1003, batch: int = 64, prefix: int = 4096,
                          extend: int = 256, pool_size: int = 1 << 21,
-                         heads=(32, 8)) -> Workload:
+                         heads=(32, 8), page_size: int = 1) -> Workload:
     """Shared system prompt: every request's row starts with the same prefix
-    slots, then extends by ``extend`` private causal tokens (GQA 32/8, d 128)."""
+    slots, then extends by ``extend`` private causal tokens (GQA 32/8, d 128).
+    With ``page_size`` > 1 (dividing ``prefix``) the prefix and each request's
+    suffix own whole pages of that many consecutive slots (``_page_runs``)."""
     dims = Dims(heads[0], heads[1], 128, pool_size, 1.0 / math.sqrt(128))
     g = _rng(seed, _S_LAYOUT + 100)
+    recipe = dict(batch=batch, prefix=prefix, extend=extend, pool=pool_size, page_size=page_size)
+    if page_size > 1:
+        assert prefix % page_size == 0, "the shared prefix must fill whole pages"
+        runs = _page_runs(g, pool_size, page_size, [prefix] + [extend] * batch)
+        shared = runs[0]
+        return build_workload("shared_prompt_extend", dims, seed,
+                              extend_prefix=[shared] * batch, extend_lens=[extend] * batch,
+                              std=1.0, slot_source=np.concatenate(runs[1:]), live_slots=shared,
+                              recipe=recipe)
     perm = g.permutation(pool_size).astype(np.int32)
     shared = perm[:prefix]
     return build_workload("shared_prompt_extend", dims, seed,
                           extend_prefix=[shared] * batch, extend_lens=[extend] * batch,
-                          std=1.0, slot_source=perm[prefix:], live_slots=shared,
-                          recipe=dict(batch=batch, prefix=prefix, extend=extend, pool=pool_size))
+                          std=1.0, slot_source=perm[prefix:], live_slots=shared, recipe=recipe)
 
 
 def tree_of_thought_decode(seed: int = 1004, depth: int = 4, fanout: int = 4,

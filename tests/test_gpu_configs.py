@@ -60,6 +60,16 @@ def test_decode_llama7b_full():
     assert_close(got[reqs], want, "decode_llama7b")
 
 
+def test_decode_llama7b_paged_full():
+    """The Llama-7B-like decode with requests owning whole pages of 64 slots."""
+    w = W.decode_llama7b(page_size=64)
+    got = Run(w).decode()
+    _check_all_finite(got, "decode paged")
+    reqs = _sample_requests(w.decode[0].seq_lens, 4, 3)
+    want = oracle_decode(w, 0, requests=reqs, pool=w.pool_view(decode_steps=1))
+    assert_close(got[reqs], want, "decode_llama7b page 64")
+
+
 def test_shared_prompt_extend_full():
     w = W.shared_prompt_extend()
     run = Run(w)

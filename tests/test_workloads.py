@@ -1,5 +1,6 @@
 """Properties of the seeded slot layouts (host only)."""
 import numpy as np
+import pytest
 
 from radixattention_prefix_shared_gb300 import workloads as W
 
@@ -120,3 +121,27 @@ def test_same_seed_same_bits():
     assert np.array_equal(a.req_to_token, b.req_to_token)
     assert np.array_equal(a.extend.q, b.extend.q)
     assert np.array_equal(a.live_k.all(), b.live_k.all())
+
+
+@pytest.mark.parametrize("page", [16, 64])
+def test_paged_layouts_own_whole_pages(page):
+    """With a page size, every request's positions fill whole pages of
+    consecutive slots (page-aligned), no page is shared between two requests
+    except the shared prompt's, and the new tokens sit inside their pages."""
+    w = W.decode_llama7b(batch=8, pool_size=1 << 16, seq_range=(100, 700), page_size=page)
+    d = w.decode[0]
+    owner = {}
+    for r in range(d.seq_lens.size):
+        row = w.req_to_token[d.req_pool_idx[r], : d.seq_lens[r]].astype(np.int64)
+        assert row[-1] == d.slots[r]
+        for k in range(0, row.size, page):
+            run = row[k: k + page]
+            assert run[0] % page == 0 and np.array_equal(run, run[0] + np.arange(run.size))
+            assert owner.setdefault(run[0] // page, r) == r
+    sp = W.shared_prompt_extend(batch=4, prefix=256, extend=40, pool_size=1 << 14, page_size=page)
+    e = sp.extend
+    assert e.slots.size == 4 * 40 and np.unique(e.slots).size == e.slots.size
+    assert np.all(e.slots.reshape(4, 40)[:, 0] % page == 0)
+    shared = sp.req_to_token[e.req_pool_idx[0], :256].astype(np.int64)
+    assert np.all(shared.reshape(-1, page)[:, 0] % page == 0)
+    assert all(np.array_equal(sp.req_to_token[r, :256], shared) for r in e.req_pool_idx)
