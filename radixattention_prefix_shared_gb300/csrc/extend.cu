@@ -19,8 +19,11 @@
 // Warp roles (19 warps):
 //   warps 0-15 softmax: Q tile t = (w/4)%2, TMEM lane quarter w%4, key-column
 //              half w/8 -- two warps share the rows of a lane quarter, each
-//              taking 64 of the block's 128 keys
-//   warps 16-17 producers: 16-byte cp.async gathers of Q, K and V rows into
+//              taking 64 of the block's 128 keys.  Idle until the first S,
+//              they also issue the Q tiles' copies; at the end they write the
+//              output through shared memory (each thread deposits its row,
+//              each warp stores whole rows with consecutive lanes)
+//   warps 16-17 producers: 16-byte cp.async gathers of K and V rows into
 //              the 128-byte-swizzled shared-memory layout the tensor core
 //              reads; each thread's arrival on the stage's mbarrier fires in
 //              hardware when its copies land (cp.async.mbarrier.arrive), so a
@@ -86,6 +89,10 @@ constexpr float kFp8Operand = 256.0f;
 #define SGL_FP8_BATCH 4
 #endif
 
+#ifndef SGL_EXTEND_Q_BY_SOFTMAX
+#define SGL_EXTEND_Q_BY_SOFTMAX 1
+#endif
+
 // warp roles: softmax warps, producer warps, the MMA warp
 // (e4m3: three producer warps; with whole-row softmax 12 warps leave 168
 // registers a thread)
@@ -99,6 +106,11 @@ struct Roles {
   static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kProducerThreads = kProducerWarps * 32;
+  // bf16 pools: the softmax warps, idle until the first S, issue the Q
+  // copies, so the producers start on K/V at once (e4m3: the producers copy
+  // and widen Q)
+  static constexpr bool kQBySoftmax = !kFp8 && SGL_EXTEND_Q_BY_SOFTMAX;
+  static constexpr int kQThreads = kQBySoftmax ? kSoftmaxWarps * 32 : kProducerThreads;
   // a producer thread copies 16-byte chunk (ptid % 8) of the bf16 rows
   // ptid / 8 + kRowStep * i < 128, i < kRowsPerThread, of every 128-row tile
   static constexpr int kRowStep = kProducerThreads / 8;
@@ -212,6 +224,75 @@ SGL_DEV bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars, int* status) 
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, &bars->abort, status);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Epilogue staging.  Once o_done has fired no MMA reads the Q tiles or the
+// K/V ring and no producer writes them, so that space holds the finished rows:
+// row rr of tile t at byte (t * 128 + rr) * stride (rows padded by 16 bytes,
+// so the 32 rows a warp deposits at once fall on different banks).  Each
+// thread deposits its own row (the TMEM lane it read); the warp then writes
+// its 32 rows out with consecutive lanes on consecutive 16-byte pieces of a
+// row, instead of every lane storing into a different row.
+template <int D>
+constexpr int out_stride() { return 2 * D + 16; }  // bf16 output rows
+
+// The warp's rows row0 .. row0+31 of a staged tile: kSeg bytes of each row at
+// stage + rr * kStride go to dst(rr) (nullptr: the row holds no output).  The
+// destination is recomputed per row from its index (measured faster than
+// broadcasting each owner's pointer by shuffle).
+template <int kSeg, int kStride, typename DstFn>
+SGL_DEV void warp_store_rows(uint32_t stage, int row0, DstFn dst) {
+  constexpr int kCpr = kSeg / 16;  // 16-byte pieces per row
+  constexpr int kRpi = 32 / kCpr;  // rows per pass of the warp
+  static_assert(kSeg % 16 == 0 && 32 % kCpr == 0, "row segment");
+  const int lane = threadIdx.x & 31;
+  __syncwarp();  // the warp's deposits are visible to the whole warp
+#pragma unroll
+  for (int i = 0; i < kCpr; ++i) {
+    const int rr = row0 + i * kRpi + lane / kCpr, c = lane % kCpr;
+    uint8_t* d = dst(rr);
+    if (d != nullptr) *reinterpret_cast<uint4*>(d + 16 * c) = ld_shared_v4(stage + rr * kStride + 16 * c);
+  }
+}
+
+// both tiles' staged rows fit in the Q tiles and the ring, below the
+// barriers
+template <int D, bool kFp8>
+constexpr bool staging_fits() {
+  using C = Cfg<D, kFp8>;
+  return 256 * out_stride<D>() <= (2 + C::kStages) * C::kTileBytes;
+}
+static_assert(staging_fits<128, false>() && staging_fits<64, false>() && staging_fits<128, true>() &&
+                  staging_fits<64, true>(),
+              "epilogue staging");
+
+// 16-byte cp.async copies of the two Q tiles into the swizzled K-major
+// layout, spread over `nthreads` threads (ltid = index among them): chunk
+// ltid % 8 of rows ltid / 8 + (nthreads / 8) * i.  Row m of tile t is token
+// q0 + t * tpt + m / g, head m % g of the KV head's group; rows past the
+// CTA's tokens are zero-filled.  Group mode gathers the members' decode
+// queries.
+template <int D, bool kGroup>
+SGL_DEV void issue_q_copies(const Params& p, uint32_t sQ_a, int ltid, int nthreads, int e, int mbeg,
+                            int q0, int off) {
+  using C = Cfg<D, false>;
+  const int kvh = blockIdx.y;
+  const int ci = ltid & 7, step = nthreads >> 3;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    for (int row = ltid >> 3; row < 128; row += step) {
+      const int tok = q0 + t * p.tpt + row / p.g;
+      bool valid = row < p.rows_used && tok < e;
+      // the query row: suffix token off+tok, or member tok's decode query
+      int64_t qrow = valid ? (kGroup ? (int64_t)p.members[mbeg + tok] : (int64_t)(off + tok)) : 0;
+      if (kGroup && (qrow < 0 || qrow >= p.batch)) valid = false, qrow = 0;
+      const __nv_bfloat16* src = p.q + (qrow * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + ci * 8;
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c)
+        cp_async_16(sQ_a + t * C::kTileBytes + c * C::kChunkBytes + sw128(row, ci),
+                    valid ? src + c * 64 : p.q, valid ? 16u : 0u);
+    }
+  }
 }
 
 // Producers on an e4m3 pool (Roles<true>::kProducerThreads threads, ptid =
@@ -427,7 +508,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     if (lane == 0) bars->red[warp] = part;
   }
   if (tid == 0) {
-    mbar_init(&bars->q_full, R::kProducerThreads);
+    mbar_init(&bars->q_full, R::kQThreads);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_ready[t], R::kSoftmaxWarps / 2 * 32);  // the softmax warps of the tile
@@ -459,6 +540,10 @@ SGL_DEV void attend_tiles(const Params& p) {
   if (R::kFullRows && warp < R::kSoftmaxWarps) {
     if constexpr (R::kFullRows) {
     // ------------------------------------------------------------ softmax (whole rows)
+    if constexpr (R::kQBySoftmax) {
+      issue_q_copies<D, kGroup>(p, sQ_a, tid, R::kQThreads, e, mbeg, q0, off);
+      cp_async_mbar_arrive(&bars->q_full);
+    }
     // warp w: Q tile t = w / 4, TMEM lane quarter q = w % 4 (rows 32q..);
     // every thread owns one row: all 128 keys of a block, all D columns of O.
     // A row whose block sum breaks the bound moves its own reference (the
@@ -565,14 +650,15 @@ SGL_DEV void attend_tiles(const Params& p) {
     if (ok) ok = warp_wait(&bars->o_done, 0, bars, p.status);
     if (ok) {
       tc_fence_after();
+      const uint32_t smem_a = smem_u32(smem);
       if constexpr (kGroup) {
         const int rm = row_valid ? p.members[mbeg + tok] : 0;
         const int dep = p.group_depth[r];
         const bool wr = row_valid && rm >= 0 && rm < p.batch && dep >= 0 && dep < p.max_depth;
         const int64_t ent =
             ((p.part_base + (int64_t)rm * p.max_depth + dep) * p.Hkv + kvh) * p.g + row % p.g;
-        float* dst = p.part_acc + ent * D;
         const float os = kFp8 ? p.o_scale : 1.f;
+        float* dst = p.part_acc + ent * D;
 #pragma unroll
         for (int j = 0; j < D / 32; ++j) {
           uint32_t o[32];
@@ -589,8 +675,8 @@ SGL_DEV void attend_tiles(const Params& p) {
         if (wr) p.part_ml[ent] = make_float2(m_ref, l);
       } else {
         const float inv = l > 0.f ? (kFp8 ? p.o_scale : 1.f) / l : 0.f;
-        __nv_bfloat16* orow =
-            p.out + ((int64_t)(off + tok) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D;
+        constexpr int kStride = out_stride<D>();
+        const uint32_t stage = smem_a + t * 128 * kStride;
 #pragma unroll
         for (int j = 0; j < D / 32; ++j) {
           uint32_t o[32];
@@ -600,19 +686,27 @@ SGL_DEV void attend_tiles(const Params& p) {
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * j);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v)
+            st_shared_v4(stage + row * kStride + 64 * j + 16 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                         w[4 * v + 3]);
         }
+        warp_store_rows<2 * D, kStride>(stage, q * 32, [&](int rr) -> uint8_t* {
+          const int tk = q0 + t * p.tpt + rr / p.g;
+          if (rr >= p.rows_used || tk >= e) return nullptr;
+          return reinterpret_cast<uint8_t*>(p.out +
+                                            ((int64_t)(off + tk) * p.Hq + (int64_t)kvh * p.g + rr % p.g) * D);
+        });
       }
     }
     }
   } else if (warp < R::kSoftmaxWarps) {
     if constexpr (!R::kFullRows) {
     // ------------------------------------------------------------ softmax
+    if constexpr (R::kQBySoftmax) {
+      issue_q_copies<D, kGroup>(p, sQ_a, tid, R::kQThreads, e, mbeg, q0, off);
+      cp_async_mbar_arrive(&bars->q_full);
+    }
     // warp w: Q tile t, key-column half h, TMEM lane quarter q (rows 32q..)
     const int t = (warp >> 2) & 1, h = warp >> 3, q = warp & 3;
     const int row = q * 32 + lane;
@@ -732,15 +826,17 @@ SGL_DEV void attend_tiles(const Params& p) {
     *xchg_mine = l;
     named_bar_sync(pair_bar, 64);
     const float lrow = *xchg_mine + *xchg_other;
+    const uint32_t smem_a = smem_u32(smem);
     if constexpr (kGroup) {
       if (ok) {
         tc_fence_after();
-        // this half writes columns [h*D/2, (h+1)*D/2) of the row's state
+        // this half holds columns [h*D/2, (h+1)*D/2) of the row's state
         const int rm = row_valid ? p.members[mbeg + tok] : 0;
         const int dep = p.group_depth[r];
         const bool wr = row_valid && rm >= 0 && rm < p.batch && dep >= 0 && dep < p.max_depth;
         const int64_t ent =
             ((p.part_base + (int64_t)rm * p.max_depth + dep) * p.Hkv + kvh) * p.g + row % p.g;
+        const float os = kFp8 ? p.o_scale : 1.f;
         float* dst = p.part_acc + ent * D + (D / 2) * h;
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
@@ -748,7 +844,6 @@ SGL_DEV void attend_tiles(const Params& p) {
           tmem_ld32(tO + (D / 2) * h + 32 * j, o);
           tmem_wait_ld();
           if (wr) {
-            const float os = kFp8 ? p.o_scale : 1.f;
             float4* d4 = reinterpret_cast<float4*>(dst + 32 * j);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -761,9 +856,9 @@ SGL_DEV void attend_tiles(const Params& p) {
     } else if (ok) {
       tc_fence_after();
       const float inv = lrow > 0.f ? (kFp8 ? p.o_scale : 1.f) / lrow : 0.f;
-      // this half writes columns [h*D/2, (h+1)*D/2) of the output row
-      __nv_bfloat16* orow =
-          p.out + ((int64_t)(off + tok) * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + (D / 2) * h;
+      // this half holds columns [h*D/2, (h+1)*D/2) of the output row
+      constexpr int kStride = out_stride<D>();
+      const uint32_t stage = smem_a + t * 128 * kStride + D * h;
 #pragma unroll
       for (int j = 0; j < D / 64; ++j) {
         uint32_t o[32];
@@ -773,13 +868,17 @@ SGL_DEV void attend_tiles(const Params& p) {
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * j);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-        }
+        for (int v = 0; v < 4; ++v)
+          st_shared_v4(stage + row * kStride + 64 * j + 16 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                       w[4 * v + 3]);
       }
+      warp_store_rows<D, kStride>(stage, q * 32, [&](int rr) -> uint8_t* {
+        const int tk = q0 + t * p.tpt + rr / p.g;
+        if (rr >= p.rows_used || tk >= e) return nullptr;
+        return reinterpret_cast<uint8_t*>(
+            p.out + ((int64_t)(off + tk) * p.Hq + (int64_t)kvh * p.g + rr % p.g) * D + (D / 2) * h);
+      });
     }
     }
   } else if (warp < R::kMmaWarp) {
@@ -792,28 +891,12 @@ SGL_DEV void attend_tiles(const Params& p) {
     const int ptid = tid - R::kSoftmaxWarps * 32;
     const int ci = ptid & 7;
     const int rbase = ptid >> 3;  // rows rbase + kRowStep * i
-    // Q tiles
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const int row = rbase + kRowStep * i;
-        const int tok = q0 + t * p.tpt + row / p.g;
-        bool valid = row < p.rows_used && tok < e;
-        // the query row: suffix token off+tok, or member tok's decode query
-        int64_t qrow = valid ? (kGroup ? (int64_t)p.members[mbeg + tok] : (int64_t)(off + tok)) : 0;
-        if (kGroup && (qrow < 0 || qrow >= p.batch)) valid = false, qrow = 0;
-        const __nv_bfloat16* src =
-            p.q + (qrow * p.Hq + (int64_t)kvh * p.g + row % p.g) * D + ci * 8;
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          cp_async_16(sQ_a + t * C::kTileBytes + c * C::kChunkBytes + sw128(row, ci),
-                      valid ? src + c * 64 : p.q, valid ? 16u : 0u);
-      }
+    if constexpr (!R::kQBySoftmax) {
+      issue_q_copies<D, kGroup>(p, sQ_a, ptid, R::kProducerThreads, e, mbeg, q0, off);
+      // each producer thread's arrival on q_full / kv_full fires when its own
+      // copies have landed (no producer ever waits for its copies)
+      cp_async_mbar_arrive(&bars->q_full);
     }
-    // each producer thread's arrival on q_full / kv_full fires when its own
-    // copies have landed (no producer ever waits for its copies)
-    cp_async_mbar_arrive(&bars->q_full);
     // group mode: the group's keys are read from its first member's row
     const int32_t* rtt =
         kGroup ? p.req_to_token + (int64_t)p.req_pool_idx[p.members[mbeg]] * p.rtt_stride +
