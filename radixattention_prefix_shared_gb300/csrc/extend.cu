@@ -106,11 +106,9 @@ struct Roles {
   static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kProducerThreads = kProducerWarps * 32;
-  // bf16 pools: the softmax warps, idle until the first S, issue the Q
-  // copies, so the producers start on K/V at once (e4m3: the producers copy
-  // and widen Q)
-  static constexpr bool kQBySoftmax = !kFp8 && SGL_EXTEND_Q_BY_SOFTMAX;
-  static constexpr int kQThreads = kQBySoftmax ? kSoftmaxWarps * 32 : kProducerThreads;
+  // the softmax warps, idle until the first S, may copy the Q tiles (e4m3
+  // pools: and widen them to f16), so the producers start on K/V at once
+  static constexpr bool kQBySoftmax = SGL_EXTEND_Q_BY_SOFTMAX;
   // a producer thread copies 16-byte chunk (ptid % 8) of the bf16 rows
   // ptid / 8 + kRowStep * i < 128, i < kRowsPerThread, of every 128-row tile
   static constexpr int kRowStep = kProducerThreads / 8;
@@ -266,6 +264,13 @@ static_assert(staging_fits<128, false>() && staging_fits<64, false>() && staging
                   staging_fits<64, true>(),
               "epilogue staging");
 
+// Whether the softmax warps load the Q tiles.  On e4m3 pools only in group
+// mode (cascade groups: a few key blocks per CTA, so the prologue counts);
+// measured there +5-7%, while on the chunked-prefill extend the producers'
+// own Q load was 1.5% faster.
+template <bool kFp8, bool kGroup>
+constexpr bool q_by_softmax() { return Roles<kFp8>::kQBySoftmax && (!kFp8 || kGroup); }
+
 // 16-byte cp.async copies of the two Q tiles into the swizzled K-major
 // layout, spread over `nthreads` threads (ltid = index among them): chunk
 // ltid % 8 of rows ltid / 8 + (nthreads / 8) * i.  Row m of tile t is token
@@ -295,6 +300,48 @@ SGL_DEV void issue_q_copies(const Params& p, uint32_t sQ_a, int ltid, int nthrea
   }
 }
 
+// e4m3 pools: the bf16 Q chunks this thread copied (the distribution of
+// issue_q_copies) widened in place to f16, the operand type of both MMAs.
+template <int D>
+SGL_DEV void widen_q_in_place(uint32_t sQ_a, int ltid, int nthreads) {
+  using C = Cfg<D, true>;
+  const int ci = ltid & 7, step = nthreads >> 3;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    for (int row = ltid >> 3; row < 128; row += step) {
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        const uint32_t a = sQ_a + t * C::kTileBytes + c * C::kChunkBytes + sw128(row, ci);
+        const uint4 w = ld_shared_v4(a);
+        const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+        uint32_t h[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          h[k] = pack_f16x2(__uint_as_float(x[k] << 16), __uint_as_float(x[k] & 0xFFFF0000u));
+        st_shared_v4(a, h[0], h[1], h[2], h[3]);
+      }
+    }
+  }
+}
+
+// The Q tiles loaded by the softmax warps (ltid = thread index among the
+// nthreads of them), signalled on q_full: on a bf16 pool each thread's
+// arrival fires when its copies land; on an e4m3 pool each thread waits for
+// its own copies, widens them and orders them for the tensor core first.
+template <int D, bool kGroup, bool kFp8>
+SGL_DEV void load_q_tiles(const Params& p, uint32_t sQ_a, uint64_t* q_full, int ltid, int nthreads, int e,
+                          int mbeg, int q0, int off) {
+  issue_q_copies<D, kGroup>(p, sQ_a, ltid, nthreads, e, mbeg, q0, off);
+  if constexpr (kFp8) {
+    cp_async_wait_all();
+    widen_q_in_place<D>(sQ_a, ltid, nthreads);
+    fence_proxy_async_smem();
+    mbar_arrive(q_full);
+  } else {
+    cp_async_mbar_arrive(q_full);
+  }
+}
+
 // Producers on an e4m3 pool (Roles<true>::kProducerThreads threads, ptid =
 // thread index among them; a thread's rows past the tile's end are
 // skipped).  Q: the bf16 rows are copied like on a bf16 pool, then widened to
@@ -313,8 +360,10 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
   using C = Cfg<D, true>;
   using R = Roles<true>;
   const int r = blockIdx.z, kvh = blockIdx.y;
-  // ---- Q tiles (bf16 rows, 16-byte chunk ci of rows rbase + kRowStep * i)
+  // ---- Q tiles (bf16 rows, 16-byte chunk ci of rows rbase + kRowStep * i),
+  // unless the softmax warps load them
   const int ci = ptid & 7, rbase = ptid >> 3;
+  if constexpr (!q_by_softmax<true, kGroup>()) {
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
 #pragma unroll
@@ -333,6 +382,7 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
     }
   }
   cp_async_commit();
+  }
   // ---- K/V codes in units u = kUnits * tile + part (rows kUnitRows * part
   // ..): 16-byte chunk rc of rows rrow + kRawRowStep * i < kUnitRows
   const int rc = ptid % C::kRawChunks, rrow = ptid / C::kRawChunks;
@@ -392,6 +442,7 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
   };
 #pragma unroll
   for (int u = 0; u < C::kRaw; ++u) issue_raw(u);
+  if constexpr (!q_by_softmax<true, kGroup>()) {
   // ---- widen Q in place once its group has landed (the units' groups may not)
   cp_async_wait<C::kRaw>();
 #pragma unroll
@@ -415,6 +466,7 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
   }
   fence_proxy_async_smem();
   mbar_arrive(&bars->q_full);
+  }
   // ---- widen every K/V tile into the ring, unit by unit
   bool ok = true;
   for (int tile = 0; tile < 2 * nb && ok; ++tile) {
@@ -487,6 +539,8 @@ SGL_DEV void attend_tiles(const Params& p) {
   Bars* bars = reinterpret_cast<Bars*>(sRaw + C::kRaw * C::kRawTileBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr bool kQSoft = q_by_softmax<kFp8, kGroup>();
+  constexpr int kQThreads = kQSoft ? R::kSoftmaxWarps * 32 : R::kProducerThreads;  // q_full arrivals
   // r: the request (extend mode) or the group (group mode); the "tokens" of
   // the Q tiles are the request's suffix tokens or the group's members
   const int r = blockIdx.z, kvh = blockIdx.y;
@@ -508,7 +562,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     if (lane == 0) bars->red[warp] = part;
   }
   if (tid == 0) {
-    mbar_init(&bars->q_full, R::kQThreads);
+    mbar_init(&bars->q_full, kQThreads);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_ready[t], R::kSoftmaxWarps / 2 * 32);  // the softmax warps of the tile
@@ -540,10 +594,8 @@ SGL_DEV void attend_tiles(const Params& p) {
   if (R::kFullRows && warp < R::kSoftmaxWarps) {
     if constexpr (R::kFullRows) {
     // ------------------------------------------------------------ softmax (whole rows)
-    if constexpr (R::kQBySoftmax) {
-      issue_q_copies<D, kGroup>(p, sQ_a, tid, R::kQThreads, e, mbeg, q0, off);
-      cp_async_mbar_arrive(&bars->q_full);
-    }
+    if constexpr (kQSoft)
+      load_q_tiles<D, kGroup, kFp8>(p, sQ_a, &bars->q_full, tid, kQThreads, e, mbeg, q0, off);
     // warp w: Q tile t = w / 4, TMEM lane quarter q = w % 4 (rows 32q..);
     // every thread owns one row: all 128 keys of a block, all D columns of O.
     // A row whose block sum breaks the bound moves its own reference (the
@@ -703,10 +755,8 @@ SGL_DEV void attend_tiles(const Params& p) {
   } else if (warp < R::kSoftmaxWarps) {
     if constexpr (!R::kFullRows) {
     // ------------------------------------------------------------ softmax
-    if constexpr (R::kQBySoftmax) {
-      issue_q_copies<D, kGroup>(p, sQ_a, tid, R::kQThreads, e, mbeg, q0, off);
-      cp_async_mbar_arrive(&bars->q_full);
-    }
+    if constexpr (kQSoft)
+      load_q_tiles<D, kGroup, kFp8>(p, sQ_a, &bars->q_full, tid, kQThreads, e, mbeg, q0, off);
     // warp w: Q tile t, key-column half h, TMEM lane quarter q (rows 32q..)
     const int t = (warp >> 2) & 1, h = warp >> 3, q = warp & 3;
     const int row = q * 32 + lane;
@@ -891,7 +941,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     const int ptid = tid - R::kSoftmaxWarps * 32;
     const int ci = ptid & 7;
     const int rbase = ptid >> 3;  // rows rbase + kRowStep * i
-    if constexpr (!R::kQBySoftmax) {
+    if constexpr (!kQSoft) {
       issue_q_copies<D, kGroup>(p, sQ_a, ptid, R::kProducerThreads, e, mbeg, q0, off);
       // each producer thread's arrival on q_full / kv_full fires when its own
       // copies have landed (no producer ever waits for its copies)
