@@ -551,6 +551,11 @@ SGL_DEV void attend_tiles(const Params& p) {
   const int q_end = min(e, q0 + 2 * p.tpt);
   const int nb_pre = (pfx + BN - 1) / BN;
   const int nb = nb_pre + (kGroup ? 0 : (q_end + BN - 1) / BN);
+  // Group mode: Q tile 1 holds no member (a cascade group of at most tpt
+  // members, most groups of a tree): its MMAs and softmax are skipped and tile
+  // 0 runs alone (tree cascade +4-5%).  Extend mode keeps both tiles: the
+  // branches cost the long extend CTAs ~1%.
+  const bool two_tiles = kGroup ? q0 + p.tpt < e : true;
   if (q0 >= e || nb <= 0) return;  // nothing to do (uniform across the CTA)
 
   // exclusive prefix sum of extend_lens: where request r's rows start
@@ -612,8 +617,8 @@ SGL_DEV void attend_tiles(const Params& p) {
     const int tok_i = row_valid ? tok : (1 << 30);  // padding rows see every key
     const float2 sc = make_float2(p.scale_log2, p.scale_log2);
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int b = 0; b < nb; ++b) {
+    bool ok = t == 0 || two_tiles;  // an empty tile's warps only meet the final barrier
+    for (int b = 0; b < nb && ok; ++b) {
       if (!warp_wait(&bars->s_full[t], b & 1, bars, p.status)) {
         ok = false;
         break;
@@ -771,7 +776,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     const int tok_i = row_valid ? tok : (1 << 30);  // padding rows see every key
     const float2 sc = make_float2(p.scale_log2, p.scale_log2);
     float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
-    bool ok = true;
+    bool ok = t == 0 || two_tiles;  // an empty tile's warps only meet the barriers
     for (int b = 0; b < nb && ok; ++b) {
       const bool ok_w = warp_wait(&bars->s_full[t], b & 1, bars, p.status);
       tc_fence_after();
@@ -1062,13 +1067,17 @@ SGL_DEV void attend_tiles(const Params& p) {
       issue_s(0, ks);
       umma_commit(&bars->s_full[0]);
       if (b > 0) {
-        if (!(ok = wait(&bars->p_ready[1], (b - 1) & 1))) break;
-        tc_fence_after();
-        issue_pv(1, vs, b > 1);
+        if (two_tiles) {
+          if (!(ok = wait(&bars->p_ready[1], (b - 1) & 1))) break;
+          tc_fence_after();
+          issue_pv(1, vs, b > 1);
+        }
         umma_commit(&bars->kv_empty[vs]);
       }
-      issue_s(1, ks);
-      umma_commit(&bars->s_full[1]);
+      if (two_tiles) {
+        issue_s(1, ks);
+        umma_commit(&bars->s_full[1]);
+      }
       umma_commit(&bars->kv_empty[ks]);
     }
     if (ok) {
@@ -1078,10 +1087,12 @@ SGL_DEV void attend_tiles(const Params& p) {
         fence_proxy_async_smem();
         tc_fence_after();
         issue_pv(0, vs, nb > 1);
-        ok = wait(&bars->p_ready[1], (nb - 1) & 1);
+        if (two_tiles) ok = wait(&bars->p_ready[1], (nb - 1) & 1);
         if (ok) {
-          tc_fence_after();
-          issue_pv(1, vs, nb > 1);
+          if (two_tiles) {
+            tc_fence_after();
+            issue_pv(1, vs, nb > 1);
+          }
           umma_commit(&bars->kv_empty[vs]);
           umma_commit(&bars->o_done);
         }
