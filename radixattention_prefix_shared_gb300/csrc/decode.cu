@@ -10,7 +10,7 @@
 //   1. plan    -- one block lists the work items (request, split): a
 //                 request's keys are cut into ceil(seq_len / 1024) runs of
 //                 near-equal length;
-//   2. split   -- a persistent grid (x: two waves of CTAs taking items from a
+//   2. split   -- a persistent grid (x: one wave of CTAs taking items from a
 //                 per-KV-head counter; y: KV head) runs
 //                 each item: the slot indices go to shared memory, K and V
 //                 rows of the KV head are gathered by 16-byte cp.async into a
@@ -869,8 +869,10 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
     const sgl_status st = launch_cascade_groups(*ga, stream);
     if (st != SGL_OK) return st;
   }
-  // two waves of CTAs (every CTA keeps taking items while any are left)
-  int64_t gx = ((int64_t)2 * blocks_per_sm * num_sms() + prm.Hkv - 1) / prm.Hkv;
+  // one wave of resident CTAs, every CTA taking items while any are left
+  // (measured against two waves: tree cascade +5.5%, Llama-7B-like decode
+  // +1.8%, chunked-mix decode kernel +1.2%)
+  int64_t gx = ((int64_t)blocks_per_sm * num_sms() + prm.Hkv - 1) / prm.Hkv;
   if (gx > max_items) gx = max_items;
   if (gx < 1) gx = 1;
   kern<<<dim3((unsigned)gx, (unsigned)prm.Hkv), kThreads, smem, stream>>>(prm);
