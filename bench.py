@@ -240,28 +240,38 @@ class Step:
         """One step; records events [start, after store, after extend, after decode].
 
         With `overlap` (and no events) the extend and the decode batches, which
-        touch different requests, run on two streams after the store and join
-        before the step ends: the decode CTAs take the SMs the extend's last
-        wave leaves idle."""
+        touch different requests, run on two streams and join before the step
+        ends: the decode CTAs take the SMs the extend's last wave leaves idle.
+        The decode follows the store; over a bf16 pool the extend does not
+        need it and starts beside it."""
         B, t, w = self.B, self.t, self.w
         torch = self.torch
         launches = 0
-        if ev is not None:
-            ev[0].record()
-        self.store(self.k_all, self.v_all, self.s_all)
-        launches += 1
-        if ev is not None:
-            ev[1].record()
         fork = self.overlap and ev is None and w.extend is not None and bool(w.decode)
         if fork:
+            # over a bf16 pool the extend reads its suffix from k_new / v_new
+            # and its prefix from rows stored by earlier steps, so it does not
+            # wait for this step's store; the decode (which reads its own new
+            # row from the pool) and the e4m3 extend (which reads its suffix
+            # back from the pool) do
             main = torch.cuda.current_stream()
             self.side.wait_stream(main)
+            self.store(self.k_all, self.v_all, self.s_all)
+            launches += 1
+            if self.fp8:
+                self.side.wait_stream(main)
             with torch.cuda.stream(self.side):
                 launches += self.run_extend()
             launches += self.run_decode()
             main.wait_stream(self.side)
             self.launches = launches
             return
+        if ev is not None:
+            ev[0].record()
+        self.store(self.k_all, self.v_all, self.s_all)
+        launches += 1
+        if ev is not None:
+            ev[1].record()
         launches += self.run_extend()
         if ev is not None:
             ev[2].record()
