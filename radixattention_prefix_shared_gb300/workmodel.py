@@ -30,24 +30,27 @@ def decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
             + 4 * n_keys + 2 * 2 * B * num_q_heads * head_dim)
 
 
-def decode_unique_bytes(req_to_token, req_pool_idx, seq_lens, num_q_heads, num_kv_heads, head_dim) -> int:
+def decode_unique_bytes(req_to_token, req_pool_idx, seq_lens, num_q_heads, num_kv_heads, head_dim,
+                        kv_elem_bytes: int = 2) -> int:
     """Like ``decode_bytes`` but counting each distinct slot once (shared
     prefixes read once)."""
     rows = [np.asarray(req_to_token[int(r), : int(s)]) for r, s in zip(req_pool_idx, seq_lens)]
     uniq = np.unique(np.concatenate(rows)).size if rows else 0
     seq = np.asarray(seq_lens, dtype=np.int64)
-    return (uniq * kv_bytes_per_token(num_kv_heads, head_dim) + 4 * int(seq.sum())
+    return (uniq * kv_bytes_per_token(num_kv_heads, head_dim, elem_bytes=kv_elem_bytes) + 4 * int(seq.sum())
             + 2 * 2 * int(seq.size) * num_q_heads * head_dim)
 
 
-def cascade_decode_bytes(group_len, shared_lens, seq_lens, num_q_heads, num_kv_heads, head_dim) -> int:
+def cascade_decode_bytes(group_len, shared_lens, seq_lens, num_q_heads, num_kv_heads, head_dim,
+                         kv_elem_bytes: int = 2) -> int:
     """Like ``decode_bytes`` with every shared group's keys read once: the K+V
-    rows and slot ids of each group's keys and of each request's private tail
-    ``[shared_len, seq_len)``, plus q in and out."""
+    rows (2-byte bf16 or 1-byte e4m3 values) and slot ids of each group's keys
+    and of each request's private tail ``[shared_len, seq_len)``, plus q in
+    and out (bf16)."""
     seq = np.asarray(seq_lens, dtype=np.int64)
     tail = np.maximum(seq - np.asarray(shared_lens, dtype=np.int64), 0)
     n_keys = int(np.sum(np.asarray(group_len, dtype=np.int64))) + int(tail.sum())
-    return (n_keys * (kv_bytes_per_token(num_kv_heads, head_dim) + 4)
+    return (n_keys * (kv_bytes_per_token(num_kv_heads, head_dim, elem_bytes=kv_elem_bytes) + 4)
             + 2 * 2 * int(seq.size) * num_q_heads * head_dim)
 
 

@@ -33,29 +33,50 @@ def test_decode_bytes_by_enumeration(elem):
     assert WM.decode_bytes(seq, 4, 2, 8, elem) == _enumerated_decode_bytes(seq, 4, 2, 8, elem)
 
 
-def test_cascade_bytes_read_each_group_once():
+@pytest.mark.parametrize("elem", [2, 1])
+def test_cascade_bytes_read_each_group_once(elem):
     # three requests share positions [0, 4) (one group), requests 0 and 1 also
     # share [4, 6) (a second group); the rest of each row is private
     seq = [9, 6, 5]
     shared = [6, 6, 4]
     groups = [4, 2]
     hq, hkv, d = 4, 2, 8
-    row = 2 * hkv * d * 2 + 4                    # K + V (bf16) + slot id per key
-    keys = sum(groups) + sum(s - sh for s, sh in zip(seq, shared))
-    want = keys * row + len(seq) * 2 * hq * d * 2
-    assert WM.cascade_decode_bytes(groups, shared, seq, hq, hkv, d) == want
+    total = 0
+    for s, sh in zip(seq, shared):
+        for _ in range(sh, s):                   # every private tail key
+            total += 2 * hkv * d * elem + 4      # K + V rows, slot id
+        total += 2 * hq * d * 2                  # bf16 query in, output out
+    for n in groups:
+        for _ in range(n):                       # every group key, once
+            total += 2 * hkv * d * elem + 4
+    assert WM.cascade_decode_bytes(groups, shared, seq, hq, hkv, d, elem) == total
     # with no sharing it is plain decode
-    assert (WM.cascade_decode_bytes([], [0, 0, 0], seq, hq, hkv, d)
-            == WM.decode_bytes(seq, hq, hkv, d))
+    assert (WM.cascade_decode_bytes([], [0, 0, 0], seq, hq, hkv, d, elem)
+            == WM.decode_bytes(seq, hq, hkv, d, elem))
 
 
-def test_decode_unique_bytes_counts_shared_slots_once():
+@pytest.mark.parametrize("elem", [2, 1])
+def test_decode_unique_bytes_counts_shared_slots_once(elem):
     rtt = np.array([[3, 4, 5, 9], [3, 4, 6, 0], [7, 8, 0, 0]], dtype=np.int32)
     seq = [4, 3, 2]
     hq, hkv, d = 2, 1, 4
     uniq = len({3, 4, 5, 9, 6, 7, 8})
-    want = uniq * 2 * hkv * d * 2 + 4 * sum(seq) + len(seq) * 2 * hq * d * 2
-    assert WM.decode_unique_bytes(rtt, [0, 1, 2], seq, hq, hkv, d) == want
+    want = uniq * 2 * hkv * d * elem + 4 * sum(seq) + len(seq) * 2 * hq * d * 2
+    assert WM.decode_unique_bytes(rtt, [0, 1, 2], seq, hq, hkv, d, elem) == want
+
+
+def test_bench_counts_e4m3_cascade_bytes_at_one_byte_a_value():
+    """The bench's read-once decode bytes over an e4m3 pool use one byte per
+    K/V value, like its plain-decode bytes."""
+    import bench
+    from radixattention_prefix_shared_gb300 import workloads as W
+    w = W.tree_of_thought_decode(pool_size=1 << 18, steps=1)
+    groups = [W.tree_groups(w, 0)]
+    b16, b8 = bench.work_of(w, groups, 2), bench.work_of(w, groups, 1)
+    qo = 2 * 2 * w.decode[0].q.shape[0] * w.dims.num_q_heads * w.dims.head_dim
+    n_keys = (b16["decode_read_once_bytes"] - qo) // (2 * w.dims.num_kv_heads * w.dims.head_dim * 2 + 4)
+    assert b8["decode_read_once_bytes"] == n_keys * (2 * w.dims.num_kv_heads * w.dims.head_dim + 4) + qo
+    assert b8["decode_read_once_bytes"] < b16["decode_read_once_bytes"]
 
 
 @pytest.mark.parametrize("elem", [2, 1])
