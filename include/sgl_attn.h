@@ -64,6 +64,24 @@ const char* sgl_status_string(sgl_status status);
 const char* sgl_version(void);
 
 /*
+ * sgl_set_device_wait_limit_ns -- limit of the on-chip waits of the extend
+ * and cascade-group kernels (failure detection; the pages have no
+ * counterpart).
+ *
+ * Each stage barrier wait of sgl_extend_attention(_fp8) and of the group
+ * pass of sgl_cascade_decode_attention(_fp8) gives up after this much wall
+ * time (default 2 s): the kernel then records a nonzero code (0x5701) in the
+ * status word of its workspace, lets its own copies and tensor-core work
+ * finish, frees its tensor memory and returns, leaving that call's output
+ * incomplete and the device usable.  A normal call's waits last
+ * microseconds; a tiny limit makes them give up on purpose, which is how the
+ * give-up path is tested.  ns == 0 restores the default.  Process-wide,
+ * applies to launches made after the call (a captured CUDA graph keeps the
+ * limit it was captured with); returns the previous limit.
+ */
+uint64_t sgl_set_device_wait_limit_ns(uint64_t ns);
+
+/*
  * sgl_store_kv -- scatter new keys and values into their pool slots.
  *
  * Computes pool_k[slots[i], :, :] = k_new[i, :, :] and
@@ -162,13 +180,18 @@ sgl_status sgl_decode_attention(const void* q, const void* pool_k, const void* p
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  *   - Every GPU that loads the library's module holds the array until the
  *     process exits.
- *   - Work whose scratch need (sgl_decode_workspace_bytes(batch, max_seq_len,
- *     dims)) exceeds SGL_DECODE_NOALLOC_SCRATCH_BYTES is rejected with
- *     SGL_ERR_WORKSPACE before anything is launched; use sgl_decode_attention
- *     with a caller workspace for it.
- *   - The first call on a device looks up the array's device address on that
- *     device (it must be the current device); make that first call before any
- *     stream capture.
+ *   - Arguments are checked exactly as sgl_decode_attention checks them,
+ *     with the same error codes (a shape the kernels are not built for is
+ *     SGL_ERR_UNSUPPORTED).  Then work whose scratch need
+ *     (sgl_decode_workspace_bytes(batch, max_seq_len, dims)) exceeds
+ *     SGL_DECODE_NOALLOC_SCRATCH_BYTES is rejected with SGL_ERR_WORKSPACE
+ *     before anything is launched; use sgl_decode_attention with a caller
+ *     workspace for it.
+ *   - The first call on a device, in each CUDA context, looks up the array's
+ *     device address there (the device must be current); make that first
+ *     call before any stream capture.  A device reset (cudaDeviceReset)
+ *     after the first call is not supported: the library's module is loaded
+ *     again at an address the cached lookup does not know.
  *   - All calls share the array and it keeps the last call's contents:
  *     calls whose kernels overlap on the GPU race and must be serialised by
  *     the caller (one stream, or explicit ordering).  No part of it needs

@@ -8,6 +8,12 @@
 
 namespace sgl {
 
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t device_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -210,6 +216,26 @@ __global__ void check_tiling_kernel(const int32_t* __restrict__ owner, int32_t b
 sgl_status last_launch() { return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA; }
 
 }  // namespace
+
+// Every host-side check of a decode call except the workspace's: dims, the
+// head-group shape the kernels are built for, sizes, pointers and alignment.
+// SGL_OK with batch == 0 means there is nothing to launch.
+sgl_status validate_decode_call(const void* q, const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* seq_lens, int32_t batch,
+                                int32_t max_seq_len, const void* out, const sgl_attn_dims* dims,
+                                float* scale) {
+  sgl_status st = check_dims(dims, scale);
+  if (st != SGL_OK) return st;
+  if (batch < 0 || max_seq_len < 0) return SGL_ERR_INVALID_ARG;
+  if (batch == 0) return SGL_OK;
+  if (max_seq_len < 1) return SGL_ERR_INVALID_ARG;
+  if (!q || !pool_k || !pool_v || !req_to_token || !req_pool_idx || !seq_lens || !out)
+    return SGL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pool_k) || !aligned16(pool_v)) return SGL_ERR_INVALID_ARG;
+  if (rtt_rows <= 0 || rtt_stride <= 0) return SGL_ERR_INVALID_ARG;
+  return decode_shape_supported(dims->num_q_heads, dims->num_kv_heads);
+}
 }  // namespace sgl
 
 using namespace sgl;
@@ -229,6 +255,10 @@ const char* sgl_status_string(sgl_status s) {
 }
 
 const char* sgl_version(void) { return "0.1.0"; }
+
+uint64_t sgl_set_device_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+}
 
 sgl_status sgl_store_kv(const void* k_new, const void* v_new, const int32_t* slots, int32_t n,
                         void* pool_k, void* pool_v, const sgl_attn_dims* dims,
@@ -405,15 +435,10 @@ sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, b
                         int32_t batch, int32_t max_seq_len, void* out, void* workspace,
                         size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
   float scale;
-  sgl_status st = check_dims(dims, &scale);
-  if (st != SGL_OK) return st;
-  if (batch < 0 || max_seq_len < 0) return SGL_ERR_INVALID_ARG;
-  if (batch == 0) return SGL_OK;
-  if (max_seq_len < 1) return SGL_ERR_INVALID_ARG;
-  if (!q || !pool_k || !pool_v || !req_to_token || !req_pool_idx || !seq_lens || !out)
-    return SGL_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(pool_k) || !aligned16(pool_v)) return SGL_ERR_INVALID_ARG;
-  if (rtt_rows <= 0 || rtt_stride <= 0) return SGL_ERR_INVALID_ARG;
+  const sgl_status st = sgl::validate_decode_call(q, pool_k, pool_v, req_to_token, rtt_rows, rtt_stride,
+                                                  req_pool_idx, seq_lens, batch, max_seq_len, out, dims,
+                                                  &scale);
+  if (st != SGL_OK || batch == 0) return st;
   const size_t need = decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads,
                                              dims->num_kv_heads, dims->head_dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))

@@ -46,25 +46,15 @@ namespace sgl {
 
 namespace {
 
-#ifndef SGL_DECODE_CHUNK
-#define SGL_DECODE_CHUNK 1024
-#endif
-#ifndef SGL_DECODE_TILE
-#define SGL_DECODE_TILE 32
-#endif
-#ifndef SGL_DECODE_STAGES
-#define SGL_DECODE_STAGES 4
-#endif
-constexpr int kChunk = SGL_DECODE_CHUNK;  // keys per work item
-// measured best for the CUDA-core path: a deeper ring of smaller tiles
-#ifndef SGL_DECODE_TILE_FMA
-#define SGL_DECODE_TILE_FMA 16
-#endif
-#ifndef SGL_DECODE_STAGES_FMA
-#define SGL_DECODE_STAGES_FMA 6
-#endif
-constexpr int kTileBf16 = SGL_DECODE_TILE;  // bf16 keys per pipeline stage (twice as many e4m3)
-constexpr int kStages = SGL_DECODE_STAGES;  // ring depth
+constexpr int kChunk = 1024;   // keys per work item
+constexpr int kTileBf16 = 32;  // tensor-core path: bf16 keys per pipeline stage (twice as many e4m3)
+constexpr int kStages = 4;     // tensor-core path: ring depth
+// the CUDA-core path (measured best there: a deeper ring of smaller tiles)
+constexpr int kTileBf16Fma = 16;
+constexpr int kStagesFma = 6;
+// resident split CTAs an SM on the tensor-core path (4 stages at 3 CTAs
+// measured against 3 stages at 4: within 0.5% on most workloads)
+constexpr int kMmaMinBlocks = 3;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -271,35 +261,21 @@ SGL_DEV void load_row_chunk(const uint8_t* p, float* f) {
   }
 }
 
-// two e4m3 codes (low byte first) -> f16x2 bits
-SGL_DEV uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-  return (uint32_t)r.x | ((uint32_t)r.y << 16);
-}
-
 template <int D, int G, int LPT>
 __host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
 
-// e4m3 operands of the tensor-core path: 1 = widened by bit placement on the
-// integer pipe (code * 2^-8 as f16, the 2^8 folded back into the scores and
-// the published sums), 0 = the hardware e4m3x2 -> f16x2 conversion
-#ifndef SGL_DECODE_FP8_WIDEN
-#define SGL_DECODE_FP8_WIDEN 1
-#endif
-#ifndef SGL_DECODE_MMA
-#define SGL_DECODE_MMA 2
-#endif
-// Which (pool type, group size) take the tensor-core path: 0 none, 1 all, 2
-// (measured best) G >= 4, or G >= 2 on an e4m3 pool.  With one or two bf16
-// query heads per KV head the 16-row MMAs carry 14-15 empty rows and the
-// CUDA-core path is faster; from four heads on the MMAs remove most of the
-// per-key instructions (tree decode 23% faster at G = 4).  Group sizes the
-// CUDA-core path is not built for (3, 5, 6, 7, 16) always take it; above 8
-// heads the MMA rows 8..15 carry heads too.
+// Which (pool type, group size) take the tensor-core path (measured best):
+// three or more query heads per KV head, or two or more on an e4m3 pool.
+// With one or two bf16 query heads per KV head the 16-row MMAs carry 14-15
+// empty rows and the CUDA-core path is faster (7-8%); from four heads on the
+// MMAs remove most of the per-key instructions (tree decode 23% faster at
+// G = 4); above 8 heads the MMA rows 8..15 carry heads too.  e4m3 operands of
+// the tensor-core path are widened by bit placement on the integer pipe
+// (code * 2^-8 as f16, the 2^8 folded back into the scores and the published
+// sums; the hardware e4m3x2 -> f16x2 conversion measured the same).
 template <typename KV, int G>
 __host__ __device__ constexpr bool use_mma() {
-  return G == 3 || G > 4 || SGL_DECODE_MMA == 1 ||
-         (SGL_DECODE_MMA == 2 && (G >= 4 || (sizeof(KV) == 1 && G >= 2)));
+  return G >= 3 || (sizeof(KV) == 1 && G >= 2);
 }
 
 // Per-warp attention state of the CUDA-core path: LPT lanes own one key, each
@@ -526,16 +502,9 @@ struct MmaState {
           : "r"(qa[ks_][0]), "r"(a1), "r"(qa[ks_][1]), "r"(a3), "r"(b0), "r"(b1));
     }
   }
-  // widened e4m3 operands hold code * 2^-8 (bit placement) or code (cvt)
-  static constexpr float kWiden = (kBytes == 1 && SGL_DECODE_FP8_WIDEN) ? 256.f : 1.f;
-  SGL_DEV static void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    if constexpr (SGL_DECODE_FP8_WIDEN) {
-      e4m3x4_to_f16x2_scaled(w, lo, hi);
-    } else {
-      lo = e4m3x2_to_f16x2(w);
-      hi = e4m3x2_to_f16x2(w >> 16);
-    }
-  }
+  // widened e4m3 operands hold code * 2^-8
+  static constexpr float kWiden = kBytes == 1 ? 256.f : 1.f;
+  SGL_DEV static void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) { e4m3x4_to_f16x2_scaled(w, lo, hi); }
   SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2_in) {
     const float scale_log2 = scale_log2_in * kWiden;
     // ---- S = q.k for this warp's KW keys, 8 at a time; sv[nb][row set][c]
@@ -673,11 +642,8 @@ struct MmaState {
 };
 
 template <int D, int G, int LPT, typename KV>
-#ifndef SGL_DECODE_MMA_MIN_BLOCKS
-#define SGL_DECODE_MMA_MIN_BLOCKS 3
-#endif
 __host__ __device__ constexpr int split_min_blocks() {
-  return use_mma<KV, G>() ? SGL_DECODE_MMA_MIN_BLOCKS : min_blocks<D, G, LPT>();
+  return use_mma<KV, G>() ? kMmaMinBlocks : min_blocks<D, G, LPT>();
 }
 
 // Ring shape of the split kernel: the tensor-core path takes 32 bf16 keys per
@@ -686,8 +652,8 @@ __host__ __device__ constexpr int split_min_blocks() {
 template <typename KV, int G>
 struct SplitRing {
   static constexpr bool kMma = use_mma<KV, G>();
-  static constexpr int kTileB = kMma ? kTileBf16 : SGL_DECODE_TILE_FMA;  // bf16 keys per stage
-  static constexpr int kDepth = kMma ? kStages : SGL_DECODE_STAGES_FMA;
+  static constexpr int kTileB = kMma ? kTileBf16 : kTileBf16Fma;  // bf16 keys per stage
+  static constexpr int kDepth = kMma ? kStages : kStagesFma;
   static constexpr int kTile = kTileB * 2 / (int)sizeof(KV);            // keys per stage
   template <int D>
   static constexpr size_t bytes() { return (size_t)kDepth * 2 * kTileB * D * 2; }
@@ -925,14 +891,22 @@ size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, in
                           cascade ? max_depth : 0, cascade, nullptr, nullptr);
 }
 
+sgl_status decode_shape_supported(int32_t num_q_heads, int32_t num_kv_heads) {
+  if (num_kv_heads <= 0) return SGL_ERR_UNSUPPORTED;
+  const int G_pool = num_q_heads / num_kv_heads;
+  if (G_pool < 1 || G_pool > 128) return SGL_ERR_UNSUPPORTED;
+  // KV heads as the kernels see them: grid y
+  if ((int64_t)num_kv_heads * kv_split_for(G_pool) > 65535) return SGL_ERR_UNSUPPORTED;
+  return SGL_OK;
+}
+
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.batch == 0) return SGL_OK;
+  if (decode_shape_supported(a.num_q_heads, a.num_kv_heads) != SGL_OK) return SGL_ERR_UNSUPPORTED;
   const int G_pool = a.num_q_heads / a.num_kv_heads;
-  if (G_pool < 1 || G_pool > 128) return SGL_ERR_UNSUPPORTED;
   const int split = kv_split_for(G_pool);
   const int G = G_pool / split;                 // query heads of a (virtual) KV head
   const int Hkv = a.num_kv_heads * split;       // KV heads as the kernels see them
-  if (Hkv > 65535) return SGL_ERR_UNSUPPORTED;  // grid y
   const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
   Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);

@@ -14,6 +14,10 @@ namespace sgl {
 // SM count of the current device (cached per device).
 int num_sms();
 
+// Limit of the extend and cascade-group kernels' bounded waits on their
+// stage barriers, for launches made from now on (sgl_set_device_wait_limit_ns).
+uint64_t device_wait_limit_ns();
+
 // Raises kernel Kern's dynamic shared memory limit to `smem` bytes and returns
 // how many of its blocks of `threads` fit on one SM (>= 1), or -1 on a CUDA
 // error.  Done once per device and kernel: later calls (including calls made
@@ -78,6 +82,16 @@ size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t num_q_
                               int32_t num_kv_heads, int32_t head_dim, bool cascade = false,
                               int32_t max_depth = 0);
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// SGL_OK when the decode kernels are built for Hq query heads over Hkv KV
+// heads (Hq % Hkv == 0 checked by the caller), else SGL_ERR_UNSUPPORTED.
+sgl_status decode_shape_supported(int32_t num_q_heads, int32_t num_kv_heads);
+// The checks sgl_decode_attention makes before it looks at its workspace
+// (api.cu); sets *scale to the effective softmax scale.
+sgl_status validate_decode_call(const void* q, const void* pool_k, const void* pool_v,
+                                const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                                const int32_t* req_pool_idx, const int32_t* seq_lens, int32_t batch,
+                                int32_t max_seq_len, const void* out, const sgl_attn_dims* dims,
+                                float* scale);
 
 // The tensor-core pass of cascade decode: per (group, KV head, block of
 // members) the members' decode queries attend to the group's keys and every

@@ -70,6 +70,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         assert np.isfinite(got).all()
         err = np.abs(got - want)
         assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+        # the same kernels on the same inputs: the results are bit-identical
+        assert np.array_equal(W.bf16_bits(out), W.bf16_bits(ref))
 
 
 def test_noalloc_refuses_work_larger_than_its_scratch():
@@ -81,3 +83,18 @@ def test_noalloc_refuses_work_larger_than_its_scratch():
     code = lib.sgl_decode_attention_noalloc(fake, fake, fake, fake, 256, 32768, fake, fake, 248, 32768,
                                             fake, ctypes.byref(d), None)
     assert code == 3  # SGL_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(16, 8, 256), (256, 1, 128)])
+def test_noalloc_reports_unbuilt_shapes_like_the_workspace_entry_point(hq, hkv, d):
+    """A shape the kernels are not built for (head_dim 256; 256 query heads on
+    one KV head) is SGL_ERR_UNSUPPORTED from both entry points, even when its
+    scratch would also exceed the fixed array."""
+    lib = B.lib()
+    dims = B.make_dims(hq, hkv, d, 1 << 22)
+    fake = ctypes.c_void_p(0x100000)       # never dereferenced: refused on the host first
+    ws = lib.sgl_decode_attention(fake, fake, fake, fake, 256, 32768, fake, fake, 248, 32768, fake,
+                                  fake, 1 << 40, ctypes.byref(dims), None)
+    na = lib.sgl_decode_attention_noalloc(fake, fake, fake, fake, 256, 32768, fake, fake, 248, 32768,
+                                          fake, ctypes.byref(dims), None)
+    assert ws == na == 2  # SGL_ERR_UNSUPPORTED
