@@ -35,6 +35,7 @@ _P = ctypes.POINTER
 _SIGS = {
     "sgl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "sgl_version": (ctypes.c_char_p, []),
+    "sgl_set_device_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "sgl_store_kv": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, _P(sgl_attn_dims), c_vp]),
     "sgl_extend_attention": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp,
                                             c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_size,

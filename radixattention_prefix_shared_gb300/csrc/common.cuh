@@ -54,32 +54,6 @@ SGL_DEV float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for two values on the FMA/ALU pipes (no MUFU), by range reduction and a
-// polynomial: x = j + f with j = round(x) read from the low mantissa bits of
-// x + 1.5*2^23 and |f| <= 1/2; 2^f = 1 + f*(c1 + f*(c2 + f*c3)), the cubic
-// fitted by exp2_fit.py (minimax relative error 1.01e-4 on [-1/2, 1/2]);
-// 2^j is added to the exponent field.  x is clamped below at -125, so a
-// masked score (-inf) gives 2^-125 instead of 0 -- negligible next to the
-// unmasked weights of the same row, which include a 1.
-constexpr float kExp2C1 = 0.6932829022407532f;
-constexpr float kExp2C2 = 0.2422109693288803f;
-constexpr float kExp2C3 = 0.055009059607982635f;
-constexpr float kExp2Magic = 12582912.0f;  // 1.5 * 2^23
-SGL_DEV float2 exp2_fma2(float2 x) {
-  x.x = fmaxf(x.x, -125.f);
-  x.y = fmaxf(x.y, -125.f);
-  const float2 magic = make_float2(kExp2Magic, kExp2Magic);
-  const float2 t = fadd2(x, magic);                                   // round(x) in low bits
-  const float2 j = fadd2(t, make_float2(-kExp2Magic, -kExp2Magic));  // round(x)
-  const float2 f = fadd2(x, make_float2(-j.x, -j.y));                 // |f| <= 1/2
-  float2 q = ffma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
-  q = ffma2(q, f, make_float2(kExp2C1, kExp2C1));
-  q = ffma2(q, f, make_float2(1.f, 1.f));
-  const int mb = __float_as_int(kExp2Magic);
-  return make_float2(__int_as_float(__float_as_int(q.x) + ((__float_as_int(t.x) - mb) << 23)),
-                     __int_as_float(__float_as_int(q.y) + ((__float_as_int(t.y) - mb) << 23)));
-}
-
 // Unpack 8 bf16 held in a uint4 into 8 floats (a bf16 is the top half of a float).
 SGL_DEV void bf16x8_to_f32(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -185,17 +159,24 @@ SGL_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 10
   return ok != 0;
 }
 
+// Default limit of a bounded wait (2 s of wall time).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time or as soon as another thread raised *abort (when
 // `abort` is given); on a timeout it raises *abort and records
 // kDevWaitTimeout in *status (when given).  Returns false when it gave up.
+// Limits under 100 us also shorten each probe's sleep and check the clock
+// after every probe.
 SGL_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
-                               uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+                               uint64_t limit_ns = kDefaultWaitNs) {
+  const bool short_limit = limit_ns < 100000ull;
+  const uint32_t hint = short_limit ? (limit_ns < 32ull ? 32u : (uint32_t)limit_ns) : 100000u;
+  if (mbar_try_wait(bar, parity, hint)) return true;
   uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 7u) == 0) {
+    if (mbar_try_wait(bar, parity, hint)) return true;
+    if ((it & 7u) == 0 || short_limit) {
       if (abort && *abort) return false;
       if (global_timer_ns() - t0 > limit_ns) {
         if (abort) *abort = 1;

@@ -64,51 +64,32 @@ namespace {
 
 constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per KV block
-// softmax layout per pool type (measured: whole rows equal on bf16 pools,
-// +10% on e4m3 pools, whose producers then share each sub-partition with two
-// softmax warps instead of four)
-#ifndef SGL_EXTEND_FULL_ROWS_BF16
-#define SGL_EXTEND_FULL_ROWS_BF16 0
-#endif
-#ifndef SGL_EXTEND_FULL_ROWS_FP8
-#define SGL_EXTEND_FULL_ROWS_FP8 1
-#endif
 constexpr uint32_t kTmemCols = 512;
 // e4m3 codes widened by bit placement hold code * 2^-8
 constexpr float kFp8Operand = 256.0f;
-#ifndef SGL_FP8_STAGES
-#define SGL_FP8_STAGES 3
-#endif
-#ifndef SGL_FP8_UNIT_ROWS
-#define SGL_FP8_UNIT_ROWS 128
-#endif
-#ifndef SGL_FP8_RAW_SLOTS
-#define SGL_FP8_RAW_SLOTS 3
-#endif
-#ifndef SGL_FP8_BATCH
-#define SGL_FP8_BATCH 4
-#endif
-
-#ifndef SGL_EXTEND_Q_BY_SOFTMAX
-#define SGL_EXTEND_Q_BY_SOFTMAX 1
-#endif
+// e4m3 pools: f16 ring stages at D = 128 (twice as many at D = 64), raw code
+// staging slots, and code rows a producer thread loads before it stores
+// (measured: 2 staging slots -15%, half-tile staging units with 4 stages -9%)
+constexpr int kFp8Stages = 3;
+constexpr int kFp8RawSlots = 3;
+constexpr int kFp8Batch = 4;
 
 // warp roles: softmax warps, producer warps, the MMA warp
 // (e4m3: three producer warps; with whole-row softmax 12 warps leave 168
 // registers a thread)
 template <bool kFp8>
 struct Roles {
-  // softmax: 8 warps owning whole rows (one thread a row, all 128 keys of a
-  // block), or 16 warps in pairs splitting each row's keys
-  static constexpr bool kFullRows = kFp8 ? SGL_EXTEND_FULL_ROWS_FP8 : SGL_EXTEND_FULL_ROWS_BF16;
+  // softmax: on e4m3 pools 8 warps owning whole rows (one thread a row, all
+  // 128 keys of a block); on bf16 pools 16 warps in pairs splitting each
+  // row's keys (measured: whole rows equal on bf16 pools, +10% on e4m3 pools,
+  // whose producers then share each sub-partition with two softmax warps
+  // instead of four)
+  static constexpr bool kFullRows = kFp8;
   static constexpr int kSoftmaxWarps = kFullRows ? 8 : 16;
   static constexpr int kProducerWarps = kFp8 ? 3 : 2;
   static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kProducerThreads = kProducerWarps * 32;
-  // the softmax warps, idle until the first S, may copy the Q tiles (e4m3
-  // pools: and widen them to f16), so the producers start on K/V at once
-  static constexpr bool kQBySoftmax = SGL_EXTEND_Q_BY_SOFTMAX;
   // a producer thread copies 16-byte chunk (ptid % 8) of the bf16 rows
   // ptid / 8 + kRowStep * i < 128, i < kRowsPerThread, of every 128-row tile
   static constexpr int kRowStep = kProducerThreads / 8;
@@ -120,11 +101,6 @@ struct Roles {
 // TMEM column of S_t and O_t
 SGL_DEV constexpr uint32_t col_s(int t) { return 128u * t; }
 SGL_DEV constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
-#ifndef SGL_FMA_EXP_PAIRS_PER8
-#define SGL_FMA_EXP_PAIRS_PER8 0
-#endif
-// of every 8 score pairs, this many are exponentiated on the FMA pipe
-constexpr int kFmaExpPairsPer8 = SGL_FMA_EXP_PAIRS_PER8;
 
 template <int D, bool kFp8>
 struct Cfg {
@@ -134,13 +110,13 @@ struct Cfg {
   // K/V ring slots of 16-bit operands (4 keep the next block's K loading
   // while the current block's last MMAs still read the slot of the one
   // before: fewer put the widening of K on the tensor core's critical path)
-  static constexpr int kStages = kFp8 ? (D == 128 ? SGL_FP8_STAGES : 2 * SGL_FP8_STAGES)
+  static constexpr int kStages = kFp8 ? (D == 128 ? kFp8Stages : 2 * kFp8Stages)
                                       : (D == 128 ? 4 : 8);
   // e4m3: staging slots of raw codes ("units" of kUnitRows rows x D bytes,
-  // unswizzled)
-  static constexpr int kUnitRows = SGL_FP8_UNIT_ROWS;
+  // unswizzled; one unit a tile)
+  static constexpr int kUnitRows = 128;
   static constexpr int kUnits = 128 / kUnitRows;  // units per tile
-  static constexpr int kRaw = kFp8 ? (D == 128 ? SGL_FP8_RAW_SLOTS : 4) : 0;
+  static constexpr int kRaw = kFp8 ? (D == 128 ? kFp8RawSlots : 4) : 0;
   static constexpr int kRawTileBytes = kUnitRows * D;
   static constexpr int kRawChunks = D / 16;  // 16-byte code chunks per row
   static constexpr int kRawRowStep = Roles<kFp8>::kProducerThreads / kRawChunks;
@@ -196,6 +172,7 @@ struct Params {
   // (group mode); 1 on a bf16 pool
   float o_scale;
   int* status;
+  uint64_t wait_ns;  // limit of every bounded wait on a stage barrier
   // group mode (cascade decode): group j covers positions
   // [group_start[j], group_start[j] + group_len[j]) of its members' rows and
   // its members are members[member_off[j] .. member_off[j+1]); the fp32 state
@@ -218,9 +195,9 @@ struct Params {
 SGL_DEV uint32_t sw128(int row, int ci) { return row * 128 + ((ci ^ (row & 7)) << 4); }
 
 // Warp-collective bounded wait: lane 0 polls, the verdict is broadcast.
-SGL_DEV bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars, int* status) {
+SGL_DEV bool warp_wait(uint64_t* bar, uint32_t parity, Bars* bars, const Params& p) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, &bars->abort, status);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, &bars->abort, p.status, p.wait_ns);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -264,12 +241,13 @@ static_assert(staging_fits<128, false>() && staging_fits<64, false>() && staging
                   staging_fits<64, true>(),
               "epilogue staging");
 
-// Whether the softmax warps load the Q tiles.  On e4m3 pools only in group
-// mode (cascade groups: a few key blocks per CTA, so the prologue counts);
-// measured there +5-7%, while on the chunked-prefill extend the producers'
-// own Q load was 1.5% faster.
+// Whether the softmax warps, idle until the first S, load the Q tiles (so
+// the producers start on K/V at once).  Always on bf16 pools; on e4m3 pools
+// only in group mode (cascade groups: a few key blocks per CTA, so the
+// prologue counts; measured there +5-7%, while on the chunked-prefill extend
+// the producers' own Q load was 1.5% faster).
 template <bool kFp8, bool kGroup>
-constexpr bool q_by_softmax() { return Roles<kFp8>::kQBySoftmax && (!kFp8 || kGroup); }
+constexpr bool q_by_softmax() { return !kFp8 || kGroup; }
 
 // 16-byte cp.async copies of the two Q tiles into the swizzled K-major
 // layout, spread over `nthreads` threads (ltid = index among them): chunk
@@ -472,7 +450,7 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
   for (int tile = 0; tile < 2 * nb && ok; ++tile) {
     const int stage = tile % C::kStages, round = tile / C::kStages;
     if (round > 0) {
-      ok = warp_wait(&bars->kv_empty[stage], (round - 1) & 1, bars, p.status);
+      ok = warp_wait(&bars->kv_empty[stage], (round - 1) & 1, bars, p);
       if (!ok) break;
     }
     // codes 16 rc .. 16 rc + 15 of a row are f16 columns of 128-byte chunk
@@ -487,7 +465,7 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
       const int u = C::kUnits * tile + part;
       cp_async_wait<C::kRaw - 1>();  // this thread's codes of unit u have landed
       const uint8_t* src0 = sRaw + (u % C::kRaw) * C::kRawTileBytes + rc * 16;
-      constexpr int kBatch = SGL_FP8_BATCH;  // loads in flight per thread
+      constexpr int kBatch = kFp8Batch;  // loads in flight per thread
 #pragma unroll
       for (int i0 = 0; i0 < C::kRawRows; i0 += kBatch) {
         uint4 w[kBatch];
@@ -619,7 +597,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     float m_ref = -INFINITY, l = 0.f;
     bool ok = t == 0 || two_tiles;  // an empty tile's warps only meet the final barrier
     for (int b = 0; b < nb && ok; ++b) {
-      if (!warp_wait(&bars->s_full[t], b & 1, bars, p.status)) {
+      if (!warp_wait(&bars->s_full[t], b & 1, bars, p)) {
         ok = false;
         break;
       }
@@ -650,12 +628,7 @@ SGL_DEV void attend_tiles(const Params& p) {
         for (int c = 0; c < BN / 2; ++c) {
           const float2 x =
               ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc, nm);
-          float2 pw;
-          if ((c & 7) >= 8 - kFmaExpPairsPer8) {
-            pw = exp2_fma2(x);
-          } else {
-            pw = make_float2(ex2(x.x), ex2(x.y));
-          }
+          const float2 pw = make_float2(ex2(x.x), ex2(x.y));
           if (c & 1) acc1 = fadd2(acc1, pw);
           else acc0 = fadd2(acc0, pw);
           sr[c] = kFp8 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
@@ -704,7 +677,7 @@ SGL_DEV void attend_tiles(const Params& p) {
       tc_fence_before();
       mbar_arrive(&bars->p_ready[t]);
     }
-    if (ok) ok = warp_wait(&bars->o_done, 0, bars, p.status);
+    if (ok) ok = warp_wait(&bars->o_done, 0, bars, p);
     if (ok) {
       tc_fence_after();
       const uint32_t smem_a = smem_u32(smem);
@@ -778,7 +751,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     float m_ref = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     bool ok = t == 0 || two_tiles;  // an empty tile's warps only meet the barriers
     for (int b = 0; b < nb && ok; ++b) {
-      const bool ok_w = warp_wait(&bars->s_full[t], b & 1, bars, p.status);
+      const bool ok_w = warp_wait(&bars->s_full[t], b & 1, bars, p);
       tc_fence_after();
       // visible keys of this block: c < limit (key index within the block)
       int limit;
@@ -805,12 +778,7 @@ SGL_DEV void attend_tiles(const Params& p) {
         for (int c = 0; c < 32; ++c) {
           const float2 x =
               ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc, nm);
-          float2 pw;
-          if ((c & 7) >= 8 - kFmaExpPairsPer8) {
-            pw = exp2_fma2(x);
-          } else {
-            pw = make_float2(ex2(x.x), ex2(x.y));
-          }
+          const float2 pw = make_float2(ex2(x.x), ex2(x.y));
           if (c & 1) acc1 = fadd2(acc1, pw);
           else acc0 = fadd2(acc0, pw);
           sr[c] = kFp8 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
@@ -876,7 +844,7 @@ SGL_DEV void attend_tiles(const Params& p) {
       tc_fence_before();
       mbar_arrive(&bars->p_ready[t]);
     }
-    if (ok) ok = warp_wait(&bars->o_done, 0, bars, p.status);
+    if (ok) ok = warp_wait(&bars->o_done, 0, bars, p);
     // every softmax warp reaches this barrier exactly once (ok or not)
     *xchg_mine = l;
     named_bar_sync(pair_bar, 64);
@@ -946,12 +914,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     const int ptid = tid - R::kSoftmaxWarps * 32;
     const int ci = ptid & 7;
     const int rbase = ptid >> 3;  // rows rbase + kRowStep * i
-    if constexpr (!kQSoft) {
-      issue_q_copies<D, kGroup>(p, sQ_a, ptid, R::kProducerThreads, e, mbeg, q0, off);
-      // each producer thread's arrival on q_full / kv_full fires when its own
-      // copies have landed (no producer ever waits for its copies)
-      cp_async_mbar_arrive(&bars->q_full);
-    }
+    static_assert(kQSoft, "on bf16 pools the softmax warps load Q");
     // group mode: the group's keys are read from its first member's row
     const int32_t* rtt =
         kGroup ? p.req_to_token + (int64_t)p.req_pool_idx[p.members[mbeg]] * p.rtt_stride +
@@ -971,7 +934,7 @@ SGL_DEV void attend_tiles(const Params& p) {
       const int b = tile >> 1, is_v = tile & 1;
       const int stage = tile % C::kStages, round = tile / C::kStages;
       if (round > 0) {
-        ok = warp_wait(&bars->kv_empty[stage], (round - 1) & 1, bars, p.status);
+        ok = warp_wait(&bars->kv_empty[stage], (round - 1) & 1, bars, p);
         if (!ok) break;
       }
       if (!is_v) {
@@ -1021,7 +984,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       for (int i = 0; i < 64; ++i)
         if (mbar_try_wait(bar, parity, 200u)) return true;
-      return mbar_wait_bounded(bar, parity, &bars->abort, p.status);
+      return mbar_wait_bounded(bar, parity, &bars->abort, p.status, p.wait_ns);
     };
     auto issue_s = [&](int t, int stage) {
 #pragma unroll
@@ -1098,12 +1061,16 @@ SGL_DEV void attend_tiles(const Params& p) {
         }
       }
     }
-    if (!ok) {
-      // let every MMA issued so far finish before TMEM is released
-      umma_commit(&bars->drain);
-      mbar_wait_bounded(&bars->drain, 0, nullptr, nullptr);
-    }
+    // every MMA issued so far finishes before TMEM is released: after a
+    // wait gave up here, and also when a softmax warp gave up waiting for
+    // o_done while the last P.V MMAs were still running (the default limit:
+    // the tensor core always finishes)
+    umma_commit(&bars->drain);
+    mbar_wait_bounded(&bars->drain, 0, nullptr, nullptr);
   }
+  // no copy into this CTA's shared memory is still in flight when it exits
+  // (the Q tiles' copies of warps that gave up waiting)
+  cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == R::kMmaWarp) {
@@ -1186,6 +1153,7 @@ sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
   prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale * kFp8Operand : 1.f);
   prm.o_scale = a.kv_fp8 ? kFp8Operand : 1.f;
   prm.status = a.status;
+  prm.wait_ns = device_wait_limit_ns();
   prm.group_start = a.group_start;
   prm.group_len = a.group_len;
   prm.group_depth = a.group_depth;
@@ -1231,6 +1199,7 @@ sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream) {
   prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale * kFp8Operand : 1.f);
   prm.o_scale = a.kv_fp8 ? a.v_scale * kFp8Operand : 1.f;
   prm.status = static_cast<int*>(a.workspace);
+  prm.wait_ns = device_wait_limit_ns();
   return a.kv_fp8 ? dispatch<true>(a.head_dim, false, prm, a.batch, a.max_extend, stream)
                   : dispatch<false>(a.head_dim, false, prm, a.batch, a.max_extend, stream);
 }

@@ -226,3 +226,14 @@ def test_product_path_has_no_oracle_or_fallback():
             if f.endswith(".py"):
                 src = open(os.path.join(root, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_wait_limit_setter_returns_the_previous_limit():
+    """sgl_set_device_wait_limit_ns is host state only: it returns the limit
+    it replaces, and 0 restores the 2 s default."""
+    from radixattention_prefix_shared_gb300 import binding as B
+    lib = B.lib()
+    default = 2_000_000_000
+    assert lib.sgl_set_device_wait_limit_ns(12345) == default
+    assert lib.sgl_set_device_wait_limit_ns(0) == 12345
+    assert lib.sgl_set_device_wait_limit_ns(0) == default
