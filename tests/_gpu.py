@@ -14,15 +14,27 @@ DEV = "cuda:0"
 
 # ------------------------------------------------------------------ helpers
 
-def assert_close(got_bits, want, what=""):
+# Full-size samples also pin the largest error against the size of the
+# outputs: at N(0,1) inputs an output row averages hundreds to thousands of V
+# rows, so its RMS is only ~0.03-0.04 and the absolute bound above is most of
+# it.  Rounding the output to bf16 alone costs up to 2^-9 of a value, and the
+# fp32 sums add far less; 5% of the sample's RMS leaves room for that while a
+# dropped or doubled key block (an error of the order of the output itself)
+# fails.
+REL_MAX_OF_RMS = 0.05
+
+
+def assert_close(got_bits, want, what="", rel_max=None):
     got = bf16_bits_to_f64(got_bits)
     assert got.shape == want.shape, (got.shape, want.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite output (a poisoned slot was read?)"
     err = np.abs(got - want)
-    assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3g}"
-    assert err.mean() <= MEAN_ABS, f"{what}: mean abs err {err.mean():.3g}"
     rms = float(np.sqrt(np.mean(want ** 2)))
     print(f"\n[parity] {what}: max abs {err.max():.3e} mean abs {err.mean():.3e} output rms {rms:.3e}")
+    assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3g}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean abs err {err.mean():.3g}"
+    if rel_max is not None:
+        assert err.max() <= rel_max * rms, f"{what}: max abs err {err.max():.3g} > {rel_max} x rms {rms:.3g}"
     return err.max(), err.mean()
 
 

@@ -18,7 +18,8 @@ from radixattention_prefix_shared_gb300 import binding as B  # noqa: E402
 from radixattention_prefix_shared_gb300 import workloads as W  # noqa: E402
 
 from _cases import decode_case, extend_case  # noqa: E402
-from _gpu import DEV, assert_close  # noqa: E402
+from _gpu import DEV, REL_MAX_OF_RMS, assert_close  # noqa: E402
+from _sampling import extreme_prefix_requests, sample_requests, tile_edge_tokens  # noqa: E402
 from test_gpu_cascade import TREES, groups_on_device  # noqa: E402
 from test_gpu_parity import DECODE_SHAPES, EXTEND_SHAPES  # noqa: E402
 
@@ -119,8 +120,8 @@ def test_decode_fp8_full_size_sampled():
     x = (got.astype(np.uint32) << 16).view(np.float32)
     assert np.isfinite(x).all()
     seq = w.decode[0].seq_lens
-    reqs = sorted({int(np.argmax(seq)), int(np.argmin(seq)), 3, 17, 40})
-    assert_close(got[reqs], oracle_fp8(w, ks, vs, requests=reqs), "decode_llama7b fp8")
+    reqs = sample_requests(seq, 16, 41)
+    assert_close(got[reqs], oracle_fp8(w, ks, vs, requests=reqs), "decode_llama7b fp8", rel_max=REL_MAX_OF_RMS)
 
 
 # ------------------------------------------------------------------ extend
@@ -231,7 +232,33 @@ def test_shared_prompt_extend_fp8_full_sampled():
     rng = np.random.default_rng(12)
     toks = np.unique(np.concatenate([[0, offs[-1] - 1, offs[5], offs[6] - 1],
                                      rng.integers(0, offs[-1], size=8)]))
-    assert_close(got[toks], oracle_extend_fp8(w, ks, vs, tokens=toks), "shared_prompt_extend fp8")
+    assert_close(got[toks], oracle_extend_fp8(w, ks, vs, tokens=toks), "shared_prompt_extend fp8",
+                 rel_max=REL_MAX_OF_RMS)
+
+
+def test_chunked_prefill_mix_fp8_full_sampled():
+    """The chunked-prefill mix at full size over an e4m3 pool, as the bench
+    runs it: every cached row, the chunks' suffix rows and the decode tokens'
+    rows stored quantised, then the extend (suffix read back from the pool)
+    and the decode.  Extend: both ends of every Q tile of the requests with
+    the longest and the shortest prefix; decode: 40 requests and the
+    extremes."""
+    w = W.chunked_prefill_mix()
+    ks, vs = 1.0 / 64, 1.0 / 64
+    pk, pv = fp8_pools(w, 1, ks, vs)
+    e = w.extend
+    B.sgl_store_kv_fp8(W.bf16_tensor(e.k_new, DEV), W.bf16_tensor(e.v_new, DEV), W.int_tensor(e.slots, DEV),
+                       pk, pv, ks, vs)
+    ext = extend_fp8(w, pk, pv, ks, vs)
+    dec = decode_fp8(w, pk, pv, ks, vs)
+    for bits, what in ((ext, "extend"), (dec, "decode")):
+        x = (bits.astype(np.uint32) << 16).view(np.float32)
+        assert np.isfinite(x).all(), what
+    toks = tile_edge_tokens(e, extreme_prefix_requests(e), w.dims.num_q_heads // w.dims.num_kv_heads)
+    assert_close(ext[toks], oracle_extend_fp8(w, ks, vs, tokens=toks), "chunked extend fp8",
+                 rel_max=REL_MAX_OF_RMS)
+    reqs = sample_requests(w.decode[0].seq_lens, 40, 7)
+    assert_close(dec[reqs], oracle_fp8(w, ks, vs, requests=reqs), "chunked decode fp8", rel_max=REL_MAX_OF_RMS)
 
 
 # ------------------------------------------------------------------ cascade
@@ -276,5 +303,5 @@ def test_tree_of_thought_cascade_fp8_full_sampled():
     got = W.bf16_bits(out)
     x = (got.astype(np.uint32) << 16).view(np.float32)
     assert np.isfinite(x).all()
-    reqs = [0, 7, 31, 63]
-    assert_close(got[reqs], oracle_fp8(w, ks, vs, requests=reqs), "tree cascade fp8")
+    reqs = sample_requests(b.seq_lens, 32, 8)
+    assert_close(got[reqs], oracle_fp8(w, ks, vs, requests=reqs), "tree cascade fp8", rel_max=REL_MAX_OF_RMS)

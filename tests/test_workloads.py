@@ -145,3 +145,28 @@ def test_paged_layouts_own_whole_pages(page):
     shared = sp.req_to_token[e.req_pool_idx[0], :256].astype(np.int64)
     assert np.all(shared.reshape(-1, page)[:, 0] % page == 0)
     assert all(np.array_equal(sp.req_to_token[r, :256], shared) for r in e.req_pool_idx)
+
+
+def test_parity_sampler_covers_every_tile_edge():
+    """The full-size extend sample holds both ends of every Q tile of the
+    chosen requests, and the decode sample keeps the extremes."""
+    from _sampling import extreme_prefix_requests, sample_requests, tile_edge_tokens
+    e = W.chunked_prefill_mix(pool_size=1 << 19, n_decode=4).extend
+    reqs = extreme_prefix_requests(e)
+    assert len(reqs) == 2
+    assert e.prefix_lens[reqs].max() == e.prefix_lens.max() and e.prefix_lens[reqs].min() == e.prefix_lens.min()
+    toks = tile_edge_tokens(e, reqs, 2)
+    assert toks.size == len(reqs) * 2 * (2048 // 64)
+    offs = np.concatenate([[0], np.cumsum(e.extend_lens)])
+    for r in reqs:
+        mine = toks[(toks >= offs[r]) & (toks < offs[r + 1])] - offs[r]
+        assert mine[0] == 0 and mine[-1] == e.extend_lens[r] - 1
+        assert set(mine[::2] % 64) == {0} and set(mine[1::2] % 64) == {63}
+    # a ragged last tile ends at the request's last token
+    class _E:
+        extend_lens = np.array([70, 5])
+        prefix_lens = np.array([0, 9])
+    assert tile_edge_tokens(_E, [0, 1], 4).tolist() == [0, 31, 32, 63, 64, 69, 70, 74]
+    assert sample_requests(np.arange(10), 20, 0) == list(range(10))
+    s = sample_requests(np.array([5, 1, 9, 3, 7, 2]), 2, 1)
+    assert 2 in s and 1 in s
