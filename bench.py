@@ -211,12 +211,12 @@ class Step:
             t["decode"][0]["v_new"] = self.v_all[n_ext:]
         self.ws_ext = B.new_workspace(256, device)
         self.out_ext = torch.empty_like(t["extend"]["q"]) if w.extend is not None else None
-        # cascade decode: the shared-prefix groups of every decode step, read
-        # off its rows once here (the host side of a serving loop keeps them
-        # in its radix tree); "auto" uses them when the batch shares prefixes
+        # cascade decode: the shared-prefix groups of every decode step, from
+        # the library's radix tree as a serving loop's host side keeps it;
+        # "auto" uses them when the batch shares prefixes
         self.groups = []
         if cascade != "off" and w.decode:
-            self.groups = [W.tree_groups(w, s) for s in range(len(w.decode))]
+            self.groups = radix_tree_groups(w)
             if cascade == "auto" and not any(g.n_groups for g in self.groups):
                 self.groups = []
         self.cascade = bool(self.groups)
@@ -430,6 +430,26 @@ def sharing_of(w: W.Workload):
     return out
 
 
+def radix_tree_groups(w: W.Workload):
+    """The shared-prefix groups of every decode step of ``w`` from the
+    library's radix tree ("Inside SGLang", Step 4: match_prefix and insert):
+    each step inserts every request's row up to its new token (slot ids stand
+    in for token ids: requests that share a prefix share its slots), looks
+    the row up for the node it ends on, and asks the tree for the groups of
+    those nodes (sgl_radix_groups)."""
+    from radixattention_prefix_shared_gb300 import binding as B
+    tree = B.RadixTree()
+    out = []
+    for b in w.decode:
+        nodes = []
+        for r, n in zip(b.req_pool_idx, b.seq_lens):
+            row = w.req_to_token[int(r), : int(n)]
+            tree.insert(row, row)
+            nodes.append(tree.match_prefix(row)[2])
+        out.append(W.CascadeGroups(*tree.groups(nodes)))
+    return out
+
+
 def work_of(w: W.Workload, groups=(), kv_elem_bytes=2):
     d = w.dims
     flops = 0
@@ -442,7 +462,7 @@ def work_of(w: W.Workload, groups=(), kv_elem_bytes=2):
                     for b in w.decode)
     # with cascade groups each shared group's keys are read once per step
     dec_unique = sum(WM.cascade_decode_bytes(g.group_len, g.shared_lens(b.q.shape[0]), b.seq_lens,
-                                             d.num_q_heads, d.num_kv_heads, d.head_dim)
+                                             d.num_q_heads, d.num_kv_heads, d.head_dim, kv_elem_bytes)
                      for g, b in zip(groups, w.decode)) if groups else dec_bytes
     n_new = (w.extend.total_extend if w.extend is not None else 0) + sum(b.q.shape[0] for b in w.decode)
     st_bytes = WM.store_kv_bytes(n_new, d.num_kv_heads, d.head_dim, kv_elem_bytes)

@@ -145,3 +145,21 @@ def test_tree_tokens_give_the_batch_hit_rate():
     w = W.tree_of_thought_decode(depth=3, fanout=2, segment=16, steps=1, pool_size=1 << 12)
     sh = bench.sharing_of(w)["decode"]
     assert sh["tree_tokens"] == (2 + 4 + 8) * 16 + 8 and sh["prompt_tokens"] == 8 * (3 * 16 + 1)
+
+
+def test_bench_groups_come_from_the_radix_tree():
+    """The bench's cascade groups (the library's radix tree, step by step)
+    equal the groups read off the rows, at every decode step of a tree
+    workload, and a batch with no shared prefix has none."""
+    import bench
+    w = W.tree_of_thought_decode(depth=3, fanout=3, segment=20, steps=4, pool_size=1 << 14)
+    got = bench.radix_tree_groups(w)
+    assert len(got) == len(w.decode)
+    for s, cg in enumerate(got):
+        ref = W.tree_groups(w, s)
+        assert cg.n_groups == ref.n_groups > 0
+        for a, b in zip((cg.group_start, cg.group_len, cg.group_depth, cg.member_off, cg.members),
+                        (ref.group_start, ref.group_len, ref.group_depth, ref.member_off, ref.members)):
+            assert np.array_equal(a, b), s
+    plain = W.decode_llama7b(pool_size=1 << 19)
+    assert all(g.n_groups == 0 for g in bench.radix_tree_groups(plain))
