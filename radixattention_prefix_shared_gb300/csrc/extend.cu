@@ -64,9 +64,10 @@ namespace {
 
 constexpr int BM = 128;  // rows per Q tile
 constexpr int BN = 128;  // keys per KV block
-constexpr uint32_t kTmemCols = 512;
 // e4m3 codes widened by bit placement hold code * 2^-8
 constexpr float kFp8Operand = 256.0f;
+// Q tiles a cascade-group CTA holds over a bf16 pool
+constexpr int kGroupTilesBf16 = 1;
 // e4m3 pools: f16 ring stages at D = 128 (twice as many at D = 64), raw code
 // staging slots, and code rows a producer thread loads before it stores
 // (measured: 2 staging slots -15%, half-tile staging units with 4 stages -9%)
@@ -76,8 +77,10 @@ constexpr int kFp8Batch = 4;
 
 // warp roles: softmax warps, producer warps, the MMA warp
 // (e4m3: three producer warps; with whole-row softmax 12 warps leave 168
-// registers a thread)
-template <bool kFp8>
+// registers a thread).  kTiles: Q tiles of 128 rows a CTA (2, ping-pong; 1
+// for the cascade group pass over bf16 pools, small enough for two CTAs an
+// SM)
+template <bool kFp8, int kTiles = 2>
 struct Roles {
   // softmax: on e4m3 pools 8 warps owning whole rows (one thread a row, all
   // 128 keys of a block); on bf16 pools 16 warps in pairs splitting each
@@ -85,7 +88,7 @@ struct Roles {
   // whose producers then share each sub-partition with two softmax warps
   // instead of four)
   static constexpr bool kFullRows = kFp8;
-  static constexpr int kSoftmaxWarps = kFullRows ? 8 : 16;
+  static constexpr int kSoftmaxWarps = (kFullRows ? 4 : 8) * kTiles;
   static constexpr int kProducerWarps = kFp8 ? 3 : 2;
   static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
@@ -98,11 +101,14 @@ struct Roles {
   // (bf16: 2^32; f16: 2^15 < 65504)
   static constexpr float kAcceptSum = kFp8 ? 32768.0f : 4294967296.0f;
 };
-// TMEM column of S_t and O_t
+// TMEM columns: S_0 .. S_{kTiles-1}, then O_0 .. O_{kTiles-1}
+template <int kTiles>
+constexpr uint32_t tmem_cols() { return 256u * kTiles; }
 SGL_DEV constexpr uint32_t col_s(int t) { return 128u * t; }
-SGL_DEV constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
+template <int kTiles>
+SGL_DEV constexpr uint32_t col_o(int t) { return 128u * kTiles + 128u * t; }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, int kTiles = 2>
 struct Cfg {
   static constexpr int kChunks = D / 64;            // 128-byte column chunks per row
   static constexpr int kChunkBytes = 128 * 128;     // 128 rows x 128 bytes
@@ -110,8 +116,11 @@ struct Cfg {
   // K/V ring slots of 16-bit operands (4 keep the next block's K loading
   // while the current block's last MMAs still read the slot of the one
   // before: fewer put the widening of K on the tensor core's critical path)
-  static constexpr int kStages = kFp8 ? (D == 128 ? kFp8Stages : 2 * kFp8Stages)
-                                      : (D == 128 ? 4 : 8);
+  // (one Q tile: two stages, which keeps two CTAs on an SM)
+  static constexpr int kStages = kTiles == 1 ? (D == 128 ? 2 : 4)
+                                 : kFp8      ? (D == 128 ? kFp8Stages : 2 * kFp8Stages)
+                                             : (D == 128 ? 4 : 8);
+  static_assert(kTiles == 2 || !kFp8, "one Q tile only over bf16 pools");
   // e4m3: staging slots of raw codes ("units" of kUnitRows rows x D bytes,
   // unswizzled; one unit a tile)
   static constexpr int kUnitRows = 128;
@@ -142,15 +151,18 @@ struct Bars {
 
 // dynamic shared memory: 1024 bytes of alignment slack, Q tiles, the K/V
 // ring, the raw code staging (e4m3), barriers
-template <int D, bool kFp8>
+template <int D, bool kFp8, int kTiles = 2>
 constexpr int smem_bytes() {
-  using C = Cfg<D, kFp8>;
-  return 1024 + (2 + C::kStages) * C::kTileBytes + C::kRaw * C::kRawTileBytes + (int)sizeof(Bars);
+  using C = Cfg<D, kFp8, kTiles>;
+  return 1024 + (kTiles + C::kStages) * C::kTileBytes + C::kRaw * C::kRawTileBytes + (int)sizeof(Bars);
 }
 static_assert(smem_bytes<128, false>() <= 227 * 1024, "extend kernel shared memory");
 static_assert(smem_bytes<64, false>() <= 227 * 1024, "extend kernel shared memory");
 static_assert(smem_bytes<128, true>() <= 227 * 1024, "extend kernel shared memory");
 static_assert(smem_bytes<64, true>() <= 227 * 1024, "extend kernel shared memory");
+// one Q tile: two CTAs on an SM
+static_assert(2 * smem_bytes<128, false, 1>() <= 228 * 1024 && 2 * smem_bytes<64, false, 1>() <= 228 * 1024,
+              "two single-tile CTAs an SM");
 
 struct Params {
   const __nv_bfloat16* q;
@@ -255,14 +267,14 @@ constexpr bool q_by_softmax() { return !kFp8 || kGroup; }
 // q0 + t * tpt + m / g, head m % g of the KV head's group; rows past the
 // CTA's tokens are zero-filled.  Group mode gathers the members' decode
 // queries.
-template <int D, bool kGroup>
+template <int D, bool kGroup, int kTiles>
 SGL_DEV void issue_q_copies(const Params& p, uint32_t sQ_a, int ltid, int nthreads, int e, int mbeg,
                             int q0, int off) {
   using C = Cfg<D, false>;
   const int kvh = blockIdx.y;
   const int ci = ltid & 7, step = nthreads >> 3;
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
+  for (int t = 0; t < kTiles; ++t) {
     for (int row = ltid >> 3; row < 128; row += step) {
       const int tok = q0 + t * p.tpt + row / p.g;
       bool valid = row < p.rows_used && tok < e;
@@ -306,10 +318,10 @@ SGL_DEV void widen_q_in_place(uint32_t sQ_a, int ltid, int nthreads) {
 // nthreads of them), signalled on q_full: on a bf16 pool each thread's
 // arrival fires when its copies land; on an e4m3 pool each thread waits for
 // its own copies, widens them and orders them for the tensor core first.
-template <int D, bool kGroup, bool kFp8>
+template <int D, bool kGroup, bool kFp8, int kTiles>
 SGL_DEV void load_q_tiles(const Params& p, uint32_t sQ_a, uint64_t* q_full, int ltid, int nthreads, int e,
                           int mbeg, int q0, int off) {
-  issue_q_copies<D, kGroup>(p, sQ_a, ltid, nthreads, e, mbeg, q0, off);
+  issue_q_copies<D, kGroup, kTiles>(p, sQ_a, ltid, nthreads, e, mbeg, q0, off);
   if constexpr (kFp8) {
     cp_async_wait_all();
     widen_q_in_place<D>(sQ_a, ltid, nthreads);
@@ -504,15 +516,16 @@ SGL_DEV void produce_fp8(const Params& p, uint32_t sQ_a, uint8_t* sKV, uint8_t* 
 // the members' decode queries and whose keys are the group's positions read
 // once from the first member's row; each row's fp32 softmax state (reference
 // max, row sum, unnormalised P.V) is written for the decode combine to merge.
-template <int D, bool kGroup, bool kFp8>
+template <int D, bool kGroup, bool kFp8, int kTiles = 2>
 SGL_DEV void attend_tiles(const Params& p) {
-  using C = Cfg<D, kFp8>;
-  using R = Roles<kFp8>;
+  using C = Cfg<D, kFp8, kTiles>;
+  using R = Roles<kFp8, kTiles>;
+  constexpr uint32_t kTmemCols = tmem_cols<kTiles>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = smem + 2 * C::kTileBytes;
+  uint8_t* sKV = smem + kTiles * C::kTileBytes;
   uint8_t* sRaw = sKV + C::kStages * C::kTileBytes;
   Bars* bars = reinterpret_cast<Bars*>(sRaw + C::kRaw * C::kRawTileBytes);
 
@@ -524,16 +537,16 @@ SGL_DEV void attend_tiles(const Params& p) {
   const int r = blockIdx.z, kvh = blockIdx.y;
   const int mbeg = kGroup ? p.member_off[r] : 0;
   const int e = kGroup ? p.member_off[r + 1] - mbeg : p.extend_lens[r];
-  const int q0 = blockIdx.x * 2 * p.tpt;                      // first token of this CTA
+  const int q0 = blockIdx.x * kTiles * p.tpt;                 // first token of this CTA
   const int pfx = kGroup ? p.group_len[r] : p.prefix_lens[r];  // keys read from the pool
-  const int q_end = min(e, q0 + 2 * p.tpt);
+  const int q_end = min(e, q0 + kTiles * p.tpt);
   const int nb_pre = (pfx + BN - 1) / BN;
   const int nb = nb_pre + (kGroup ? 0 : (q_end + BN - 1) / BN);
   // Group mode: Q tile 1 holds no member (a cascade group of at most tpt
   // members, most groups of a tree): its MMAs and softmax are skipped and tile
   // 0 runs alone (tree cascade +4-5%).  Extend mode keeps both tiles: the
   // branches cost the long extend CTAs ~1%.
-  const bool two_tiles = kGroup ? q0 + p.tpt < e : true;
+  const bool two_tiles = kTiles == 2 && (kGroup ? q0 + p.tpt < e : true);
   if (q0 >= e || nb <= 0) return;  // nothing to do (uniform across the CTA)
 
   // exclusive prefix sum of extend_lens: where request r's rows start
@@ -548,7 +561,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     mbar_init(&bars->q_full, kQThreads);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_ready[t], R::kSoftmaxWarps / 2 * 32);  // the softmax warps of the tile
+      mbar_init(&bars->p_ready[t], R::kSoftmaxWarps / kTiles * 32);  // the softmax warps of the tile
     }
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
@@ -578,7 +591,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     if constexpr (R::kFullRows) {
     // ------------------------------------------------------------ softmax (whole rows)
     if constexpr (kQSoft)
-      load_q_tiles<D, kGroup, kFp8>(p, sQ_a, &bars->q_full, tid, kQThreads, e, mbeg, q0, off);
+      load_q_tiles<D, kGroup, kFp8, kTiles>(p, sQ_a, &bars->q_full, tid, kQThreads, e, mbeg, q0, off);
     // warp w: Q tile t = w / 4, TMEM lane quarter q = w % 4 (rows 32q..);
     // every thread owns one row: all 128 keys of a block, all D columns of O.
     // A row whose block sum breaks the bound moves its own reference (the
@@ -589,7 +602,7 @@ SGL_DEV void attend_tiles(const Params& p) {
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t tS = tmem + lane_off + col_s(t);
-    const uint32_t tO = tmem + lane_off + col_o(t);
+    const uint32_t tO = tmem + lane_off + col_o<kTiles>(t);
     const int tok = q0 + t * p.tpt + row / p.g;
     const bool row_valid = row < p.rows_used && tok < e;
     const int tok_i = row_valid ? tok : (1 << 30);  // padding rows see every key
@@ -734,13 +747,13 @@ SGL_DEV void attend_tiles(const Params& p) {
     if constexpr (!R::kFullRows) {
     // ------------------------------------------------------------ softmax
     if constexpr (kQSoft)
-      load_q_tiles<D, kGroup, kFp8>(p, sQ_a, &bars->q_full, tid, kQThreads, e, mbeg, q0, off);
+      load_q_tiles<D, kGroup, kFp8, kTiles>(p, sQ_a, &bars->q_full, tid, kQThreads, e, mbeg, q0, off);
     // warp w: Q tile t, key-column half h, TMEM lane quarter q (rows 32q..)
-    const int t = (warp >> 2) & 1, h = warp >> 3, q = warp & 3;
+    const int t = (warp >> 2) % kTiles, h = warp / (4 * kTiles), q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t tS = tmem + lane_off + col_s(t);
-    const uint32_t tO = tmem + lane_off + col_o(t);
+    const uint32_t tO = tmem + lane_off + col_o<kTiles>(t);
     const uint32_t pair_bar = 1 + t * 4 + q;  // named barrier of the two halves of these rows
     float* xchg_mine = &bars->xchg[t][h][row];
     const float* xchg_other = &bars->xchg[t][h ^ 1][row];
@@ -1000,7 +1013,7 @@ SGL_DEV void attend_tiles(const Params& p) {
       for (int kk = 0; kk < BN / 16; ++kk) {
         const uint64_t bd =
             make_sw128_desc(sKV_a + stage * C::kTileBytes + kk * 16 * 128, C::kChunkBytes, 1024);
-        umma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bd, idO, (acc || kk > 0) ? 1u : 0u);
+        umma_ts(tmem + col_o<kTiles>(t), tmem + col_s(t) + kk * 8, bd, idO, (acc || kk > 0) ? 1u : 0u);
       }
     };
     // copies landed by cp.async (generic proxy) are read by the tensor core
@@ -1084,9 +1097,11 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1) extend_kernel(Params
   attend_tiles<D, false, kFp8>(p);
 }
 
-template <int D, bool kFp8>
-__global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1) cascade_group_kernel(Params p) {
-  attend_tiles<D, true, kFp8>(p);
+// one Q tile: two CTAs an SM (11 warps a CTA are allocated registers as 12,
+// which leaves 80 registers a thread)
+template <int D, bool kFp8, int kTiles>
+__global__ void __launch_bounds__(Roles<kFp8, kTiles>::kThreads, 3 - kTiles) cascade_group_kernel(Params p) {
+  attend_tiles<D, true, kFp8, kTiles>(p);
 }
 
 template <int D, bool kFp8>
@@ -1105,11 +1120,14 @@ sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_
 template <int D, bool kFp8>
 sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members,
                       cudaStream_t stream) {
-  constexpr int kThreads = Roles<kFp8>::kThreads;
-  constexpr int kSmem = smem_bytes<D, kFp8>();
-  auto kern = cascade_group_kernel<D, kFp8>;
-  if (kernel_blocks_per_sm<cascade_group_kernel<D, kFp8>>(kSmem, kThreads) < 0) return SGL_ERR_CUDA;
-  const int per_cta = 2 * prm.tpt;
+  // bf16 pools: one Q tile a CTA, two CTAs an SM (most groups of a tree fill
+  // one tile; the second CTA's work hides each CTA's start and end)
+  constexpr int kTiles = kFp8 ? 2 : kGroupTilesBf16;
+  constexpr int kThreads = Roles<kFp8, kTiles>::kThreads;
+  constexpr int kSmem = smem_bytes<D, kFp8, kTiles>();
+  auto kern = cascade_group_kernel<D, kFp8, kTiles>;
+  if (kernel_blocks_per_sm<cascade_group_kernel<D, kFp8, kTiles>>(kSmem, kThreads) < 0) return SGL_ERR_CUDA;
+  const int per_cta = kTiles * prm.tpt;
   const unsigned gx = (unsigned)((max_members + per_cta - 1) / per_cta);
   dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)n_groups);
   kern<<<grid, kThreads, kSmem, stream>>>(prm);
