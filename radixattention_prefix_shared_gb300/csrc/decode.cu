@@ -273,9 +273,10 @@ __host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 
 // the tensor-core path are widened by bit placement on the integer pipe
 // (code * 2^-8 as f16, the 2^8 folded back into the scores and the published
 // sums; the hardware e4m3x2 -> f16x2 conversion measured the same).
+constexpr int kFp8MmaMinG = 2;
 template <typename KV, int G>
 __host__ __device__ constexpr bool use_mma() {
-  return G >= 3 || (sizeof(KV) == 1 && G >= 2);
+  return G >= 3 || (sizeof(KV) == 1 && G >= kFp8MmaMinG);
 }
 
 // Per-warp attention state of the CUDA-core path: LPT lanes own one key, each
@@ -436,7 +437,19 @@ struct MmaState {
   static constexpr int NR = kTwoRows ? 2 : 1;  // rows of a lane: g (and g + 8)
   static_assert(G <= 16, "at most 16 query heads per KV head");
   static_assert(KW == (kBytes == 2 ? 8 : 16), "stage shape");
+  // e4m3 pools with 1, 2 or 4 query heads per KV head: the K codes go to the
+  // tensor core as they are (m16n8k32 e4m3 MMAs, no widening), and the A
+  // rows hold each head's query as three e4m3 terms (hi + mid + lo: ~12
+  // significant bits, the head scaled by a power of two into e4m3's range),
+  // term j of head h in row j * G + h, so one MMA computes all three.  Lane
+  // g's rows are g and g + 8: with G <= 2 head g's terms are the rows g, g +
+  // G, g + 2G of lanes 4G and 8G on (two shuffles add them); with G = 4 they
+  // are rows g and g + 8 of the lane itself and row g + 4 of the lane 16 on.
+  static constexpr bool kDirectK = kBytes == 1 && (G <= 2 || G == 4);
+  static constexpr int KS8 = D / 32;         // k-steps of the e4m3 q.k
   uint32_t qa[KS][2 * NR];  // per k-step: row g lo, row g hi (, row g+8 lo, row g+8 hi)
+  uint32_t q8[KS8][4];      // direct K: a0..a3 of k-step ks (rows g, g + 8; k = 4t.., 16 + 4t..)
+  float qmul;               // direct K: 2^-e of head g (rows g < G)
   float o[SB][4][4];        // c0, c1: row g; c2, c3: row g + 8
   float m[NR], l[NR];
   int g, t, warp;
@@ -447,6 +460,10 @@ struct MmaState {
     warp = w;
   }
   SGL_DEV void load_q(const __nv_bfloat16* qb, float) {
+    if constexpr (kDirectK) {
+      load_q_terms(qb);
+      return;
+    }
 #pragma unroll
     for (int rr = 0; rr < NR; ++rr) {
       const int row = g + 8 * rr;
@@ -468,6 +485,66 @@ struct MmaState {
         }
       }
     }
+  }
+  // Row g = j * G + h (j < 3): term j of head h, over this lane's dims
+  // DL * t .. DL * t + DL - 1 (the same dims its K loads cover), in k-step
+  // order: k-step ks holds dims 8 ks .. 8 ks + 7 of the slice, four a word.
+  // The head's scale 2^e puts its largest |q| in [128, 256) (the four lanes of
+  // a row hold its four slices); hi = e4m3(q 2^e), mid = e4m3(q 2^e - hi),
+  // lo = e4m3(q 2^e - hi - mid), each difference exact in fp32.
+  SGL_DEV void load_q_terms(const __nv_bfloat16* qb) {
+    // rows g and g + 8 belong to the same head (G divides 8) as terms
+    // g / G and (g + 8) / G
+    const int h = g % G, term0 = g / G, term1 = (g + 8) / G;
+    const bool live = g < 3 * G;
+    float x[DL];
+    float amax = 0.f;
+#pragma unroll
+    for (int v = 0; v < DL / 8; ++v) {
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (live) raw = *reinterpret_cast<const uint4*>(qb + h * D + DL * t + 8 * v);
+      bf16x8_to_f32(raw, &x[8 * v]);
+    }
+#pragma unroll
+    for (int i = 0; i < DL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int e = 0;
+    if (amax > 0.f) e = min(126, max(-126, 7 - (((__float_as_int(amax) >> 23) & 0xff) - 127)));
+    const float sc = __int_as_float((e + 127) << 23);
+    qmul = __int_as_float((127 - e) << 23);
+#pragma unroll
+    for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+          const int d = 8 * ks + 4 * hf + i;
+          float2 v = make_float2(x[d] * sc, x[d + 1] * sc);
+          uint32_t c0 = 0u, c1 = 0u;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const __nv_fp8x2_storage_t cj = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+            if (j == term0) c0 = (uint32_t)cj;
+            if (j == term1) c1 = (uint32_t)cj;
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(cj, __NV_E4M3);
+            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            v = make_float2(v.x - back.x, v.y - back.y);
+          }
+          w0 |= c0 << (8 * i);
+          w1 |= c1 << (8 * i);
+        }
+        q8[ks][2 * hf] = live ? w0 : 0u;                      // row g
+        q8[ks][2 * hf + 1] = live && term1 < 3 ? w1 : 0u;     // row g + 8
+      }
+  }
+  SGL_DEV void qk8(float (&d4)[4], int ks_, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
+        : "r"(q8[ks_][0]), "r"(q8[ks_][1]), "r"(q8[ks_][2]), "r"(q8[ks_][3]), "r"(b0), "r"(b1));
   }
   SGL_DEV void reset() {
 #pragma unroll
@@ -506,14 +583,32 @@ struct MmaState {
   static constexpr float kWiden = kBytes == 1 ? 256.f : 1.f;
   SGL_DEV static void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) { e4m3x4_to_f16x2_scaled(w, lo, hi); }
   SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2_in) {
-    const float scale_log2 = scale_log2_in * kWiden;
+    // widened K codes hold code * 2^-8; the direct path's scores carry the
+    // head's 2^e
+    const float scale_log2 = scale_log2_in * (kDirectK ? qmul : kWiden);
     // ---- S = q.k for this warp's KW keys, 8 at a time; sv[nb][row set][c]
     float sv[KW / 8][NR][2];
 #pragma unroll
     for (int nb = 0; nb < KW / 8; ++nb) {
       const uint8_t* row = ks + (warp * KW + nb * 8 + g) * kRowBytes + DL * t * kBytes;
       float d4[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (kBytes == 2) {
+      if constexpr (kDirectK) {
+#pragma unroll
+        for (int v = 0; v < DL / 16; ++v) {  // 16 codes = two e4m3 k-steps
+          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
+          qk8(d4, 2 * v, w.x, w.y);
+          qk8(d4, 2 * v + 1, w.z, w.w);
+        }
+        // add head g's three term rows (rows past the terms hold zeros; lanes
+        // of rows >= G hold no head)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if constexpr (G == 4)
+            d4[c] += __shfl_down_sync(0xffffffffu, d4[c], 16) + d4[c + 2];
+          else
+            d4[c] += __shfl_down_sync(0xffffffffu, d4[c], 4 * G) + __shfl_down_sync(0xffffffffu, d4[c], 8 * G);
+        }
+      } else if constexpr (kBytes == 2) {
 #pragma unroll
         for (int v = 0; v < DL / 8; ++v) {  // 8 bf16 = two k-steps
           const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
