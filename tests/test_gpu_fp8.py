@@ -101,6 +101,35 @@ def test_decode_fp8_matches_oracle(shape):
     assert_close(decode_fp8(w, pk, pv, ks, vs), oracle_fp8(w, ks, vs), f"decode fp8 {shape}")
 
 
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 2)])
+def test_decode_fp8_wide_scores(hq, hkv):
+    """Scores spread over tens of natural-log units (unit-variance q and k, a
+    large softmax scale): with two or four query heads per KV head the K
+    codes meet the query as three e4m3 terms in the tensor core, whose
+    rounding the large scores would magnify -- the output must still match."""
+    w = decode_case(61 + hq, Hq=hq, Hkv=hkv, D=128, seq_lens=[900, 333, 2000, 1], scale=0.8)
+    ks, vs = 1.0 / 32, 1.0 / 32
+    pk, pv = fp8_pools(w, 1, ks, vs)
+    assert_close(decode_fp8(w, pk, pv, ks, vs), oracle_fp8(w, ks, vs), f"decode fp8 wide scores {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8)])
+def test_decode_fp8_query_range(hq, hkv):
+    """Queries whose dims span six orders of magnitude (a few dims 300x,
+    half of them 1/1000x): each head's query is scaled by a power of two into
+    e4m3's range before its three terms are taken."""
+    w = decode_case(71 + hq, Hq=hq, Hkv=hkv, D=128, seq_lens=[700, 64, 1500])
+    b = w.decode[0]
+    q = (b.q.astype(np.uint32) << 16).view(np.float32).copy()
+    q[..., :4] *= 300.0
+    q[..., 64:] *= 1e-3
+    q[1] *= 1e-20                    # one request's queries far below e4m3's range
+    b.q[...] = W.f32_to_bf16_bits(q)
+    ks, vs = 1.0 / 32, 1.0 / 32
+    pk, pv = fp8_pools(w, 1, ks, vs)
+    assert_close(decode_fp8(w, pk, pv, ks, vs), oracle_fp8(w, ks, vs), f"decode fp8 query range {hq}/{hkv}")
+
+
 def test_decode_fp8_single_key_bit_exact():
     w = decode_case(9, Hq=8, Hkv=2, D=128, seq_lens=[1, 1, 1])
     ks, vs = 1.0 / 16, 1.0 / 8         # powers of two: code * scale is exact in bf16

@@ -101,6 +101,7 @@ DECODE_SHAPES = [
     (8, 1, 128, [600, 1]),
     (16, 2, 64, [530, 64]),
     (4, 1, 64, [1500]),
+    (4, 2, 64, [700, 3, 1025]),
     # group sizes without a CUDA-core build: tensor-core rows (3, 5, 6, 7; 16 uses rows 8..15)
     (6, 2, 128, [700, 1, 33]),
     (10, 2, 128, [1500, 17]),
