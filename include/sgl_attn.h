@@ -206,6 +206,42 @@ sgl_status sgl_decode_attention_noalloc(const void* q, const void* pool_k, const
                                         sgl_stream_t stream);
 
 /*
+ * sgl_mixed_attention -- the extend batch and the decode batch of one step in
+ * one launch ("Inside SGLang", Step 10: Split long prompts into chunks: a
+ * prefill chunk and the running requests' decode tokens share a forward pass;
+ * "A walkthrough of SGLang": the MIXED forward mode).
+ *
+ * Computes exactly what sgl_extend_attention (the q_ext .. out_ext arguments,
+ * ext_workspace as its workspace) and sgl_decode_attention (q_dec .. out_dec,
+ * dec_workspace) compute over the same bf16 pools and req_to_token -- the same
+ * kernels' arithmetic on the same tiles and work items, so the outputs are
+ * those two calls' outputs bit for bit.  The extend is bound by the tensor
+ * cores and the decode by HBM bandwidth; here they share the GPU's SMs in one
+ * persistent launch: extend_sms SMs start on extend tiles, the others on
+ * decode work, and an SM whose side has run out takes the other side's work.
+ * extend_sms = 0 picks the split from the host values (half the maxima taken
+ * as mean lengths); 0 < extend_sms < the SM count sets it.
+ *   - The pools are bf16; the argument checks, preconditions, error codes and
+ *     workspace sizes are those of the two calls (ext_workspace >=
+ *     sgl_extend_workspace_bytes, its first 256 bytes zero-filled once before
+ *     first use: word 0 is the extend's bounded-wait status, words 1..3 the
+ *     launch's work counters, reset by the launch itself).
+ *   - Either batch may be empty (the other call alone runs).  Decode groups of
+ *     1 or 2 query heads per KV head at head_dim 64 or 128 run in the single
+ *     launch; other shapes run the two calls' kernels one after the other.
+ *   - The store of the step's new K/V (sgl_store_kv) must precede the call, as
+ *     for a decode.
+ */
+sgl_status sgl_mixed_attention(
+    const void* q_ext, const void* k_new, const void* v_new, const int32_t* ext_req_pool_idx,
+    const int32_t* prefix_lens, const int32_t* extend_lens, int32_t ext_batch, int32_t total_extend,
+    int32_t max_extend, int32_t max_prefix, void* out_ext, void* ext_workspace, size_t ext_workspace_bytes,
+    const void* q_dec, const int32_t* dec_req_pool_idx, const int32_t* seq_lens, int32_t dec_batch,
+    int32_t max_seq_len, void* out_dec, void* dec_workspace, size_t dec_workspace_bytes, const void* pool_k,
+    const void* pool_v, const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride, int32_t extend_sms,
+    const sgl_attn_dims* dims, sgl_stream_t stream);
+
+/*
  * sgl_cascade_decode_attention -- decode attention that reads each shared
  * prefix once per group of requests.
  *

@@ -44,6 +44,10 @@ _SIGS = {
                                             c_i32, c_vp, c_vp, c_size, _P(sgl_attn_dims), c_vp]),
     "sgl_decode_attention_noalloc": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_i32,
                                                     c_i32, c_vp, _P(sgl_attn_dims), c_vp]),
+    "sgl_mixed_attention": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
+                                           c_vp, c_vp, c_size, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp,
+                                           c_size, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, _P(sgl_attn_dims),
+                                           c_vp]),
     "sgl_extend_workspace_bytes": (c_size, [c_i32, c_i32, _P(sgl_attn_dims)]),
     "sgl_decode_workspace_bytes": (c_size, [c_i32, c_i32, _P(sgl_attn_dims)]),
     "sgl_check_store_kv_indices": (ctypes.c_int, [c_vp, c_i32, c_i64, c_vp, c_size, c_vp, c_vp]),
@@ -178,6 +182,35 @@ def sgl_extend_attention(q, k_new, v_new, pool_k, pool_v, req_to_token, req_pool
         _ptr(extend_lens), B, T, int(max_extend), int(max_prefix), _ptr(out), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), ctypes.byref(d), _stream(stream)))
     return out
+
+
+def sgl_mixed_attention(q_ext, k_new, v_new, ext_req_pool_idx, prefix_lens, extend_lens, q_dec,
+                        dec_req_pool_idx, seq_lens, pool_k, pool_v, req_to_token, out_ext=None, out_dec=None, *,
+                        max_extend, max_prefix=0, max_seq_len, total_extend=None, ext_workspace=None,
+                        dec_workspace=None, extend_sms=0, sm_scale=0.0, stream=None):
+    """An extend batch and a decode batch over the same pools in one launch
+    (outputs equal to sgl_extend_attention's and sgl_decode_attention's)."""
+    import torch
+    T = int(q_ext.shape[0]) if total_extend is None else int(total_extend)
+    d = _dims_for(q_ext, pool_k, sm_scale)
+    Be, Bd = int(ext_req_pool_idx.shape[0]), int(q_dec.shape[0])
+    if out_ext is None:
+        out_ext = torch.empty_like(q_ext)
+    if out_dec is None:
+        out_dec = torch.empty_like(q_dec)
+    if ext_workspace is None:
+        ext_workspace = new_workspace(extend_workspace_bytes(Be, T, d), q_ext.device)
+    if dec_workspace is None:
+        dec_workspace = new_workspace(decode_workspace_bytes(Bd, max_seq_len, d), q_dec.device)
+    _check("sgl_mixed_attention", lib().sgl_mixed_attention(
+        _ptr(q_ext), _ptr(k_new), _ptr(v_new), _ptr(ext_req_pool_idx), _ptr(prefix_lens), _ptr(extend_lens),
+        Be, T, int(max_extend), int(max_prefix), _ptr(out_ext), _ptr(ext_workspace),
+        int(ext_workspace.numel() * ext_workspace.element_size()), _ptr(q_dec), _ptr(dec_req_pool_idx),
+        _ptr(seq_lens), Bd, int(max_seq_len), _ptr(out_dec), _ptr(dec_workspace),
+        int(dec_workspace.numel() * dec_workspace.element_size()), _ptr(pool_k), _ptr(pool_v),
+        _ptr(req_to_token), int(req_to_token.shape[0]), int(req_to_token.shape[1]), int(extend_sms),
+        ctypes.byref(d), _stream(stream)))
+    return out_ext, out_dec
 
 
 def sgl_decode_attention(q, pool_k, pool_v, req_to_token, req_pool_idx, seq_lens, out=None, *,

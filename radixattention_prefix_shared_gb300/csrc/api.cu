@@ -317,18 +317,20 @@ size_t sgl_cascade_decode_workspace_bytes(int32_t batch, int32_t max_seq_len, in
 
 namespace {
 // k_new / v_new are null on an e4m3 pool (the suffix is read from the pool)
-sgl_status extend_entry(const void* q, const void* k_new, const void* v_new, const void* pool_k,
-                        const void* pool_v, bool kv_fp8, float k_scale, float v_scale,
-                        const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
-                        const int32_t* req_pool_idx, const int32_t* prefix_lens,
-                        const int32_t* extend_lens, int32_t batch, int32_t total_extend,
-                        int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
-                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+// Host checks of an extend call; fills *a.  *empty: nothing to launch.
+sgl_status extend_args(const void* q, const void* k_new, const void* v_new, const void* pool_k,
+                       const void* pool_v, bool kv_fp8, float k_scale, float v_scale,
+                       const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                       const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                       const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                       int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
+                       size_t workspace_bytes, const sgl_attn_dims* dims, ExtendArgs* ap, bool* empty) {
   float scale;
   sgl_status st = check_dims(dims, &scale);
   if (st != SGL_OK) return st;
   if (batch < 0 || total_extend < 0 || max_extend < 0 || max_prefix < 0) return SGL_ERR_INVALID_ARG;
-  if (batch == 0 || total_extend == 0) return SGL_OK;
+  *empty = batch == 0 || total_extend == 0;
+  if (*empty) return SGL_OK;
   if (!kv_fp8 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
     return SGL_ERR_INVALID_ARG;
   if (!q || !pool_k || !pool_v || !req_to_token || !req_pool_idx || !prefix_lens || !extend_lens ||
@@ -339,7 +341,7 @@ sgl_status extend_entry(const void* q, const void* k_new, const void* v_new, con
   if (rtt_rows <= 0 || rtt_stride <= 0 || max_extend > total_extend) return SGL_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < extend_workspace_bytes() || !aligned16(workspace))
     return SGL_ERR_WORKSPACE;
-  ExtendArgs a;
+  ExtendArgs& a = *ap;
   a.q = q;
   a.k_new = k_new;
   a.v_new = v_new;
@@ -363,6 +365,23 @@ sgl_status extend_entry(const void* q, const void* k_new, const void* v_new, con
   a.kv_fp8 = kv_fp8;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  return SGL_OK;
+}
+
+sgl_status extend_entry(const void* q, const void* k_new, const void* v_new, const void* pool_k,
+                        const void* pool_v, bool kv_fp8, float k_scale, float v_scale,
+                        const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride,
+                        const int32_t* req_pool_idx, const int32_t* prefix_lens,
+                        const int32_t* extend_lens, int32_t batch, int32_t total_extend,
+                        int32_t max_extend, int32_t max_prefix, void* out, void* workspace,
+                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+  ExtendArgs a;
+  bool empty = false;
+  const sgl_status st = extend_args(q, k_new, v_new, pool_k, pool_v, kv_fp8, k_scale, v_scale, req_to_token,
+                                    rtt_rows, rtt_stride, req_pool_idx, prefix_lens, extend_lens, batch,
+                                    total_extend, max_extend, max_prefix, out, workspace, workspace_bytes,
+                                    dims, &a, &empty);
+  if (st != SGL_OK || empty) return st;
   return launch_extend(a, reinterpret_cast<cudaStream_t>(stream));
 }
 }  // namespace
@@ -429,21 +448,24 @@ sgl_status sgl_decode_attention_fp8(const void* q, const void* pool_k, const voi
 }
 
 namespace {
-sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, bool kv_fp8,
-                        float k_scale, float v_scale, const int32_t* req_to_token, int32_t rtt_rows,
-                        int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
-                        int32_t batch, int32_t max_seq_len, void* out, void* workspace,
-                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+// Host checks of a decode call; fills *a.  *empty: nothing to launch.
+sgl_status decode_args(const void* q, const void* pool_k, const void* pool_v, bool kv_fp8,
+                       float k_scale, float v_scale, const int32_t* req_to_token, int32_t rtt_rows,
+                       int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+                       int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                       size_t workspace_bytes, const sgl_attn_dims* dims, DecodeArgs* ap, bool* empty) {
   float scale;
   const sgl_status st = sgl::validate_decode_call(q, pool_k, pool_v, req_to_token, rtt_rows, rtt_stride,
                                                   req_pool_idx, seq_lens, batch, max_seq_len, out, dims,
                                                   &scale);
-  if (st != SGL_OK || batch == 0) return st;
+  *empty = batch == 0;
+  if (st != SGL_OK || *empty) return st;
   const size_t need = decode_workspace_bytes(batch, max_seq_len, dims->num_q_heads,
                                              dims->num_kv_heads, dims->head_dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
     return SGL_ERR_WORKSPACE;
-  DecodeArgs a;
+  DecodeArgs& a = *ap;
+  a = DecodeArgs{};
   a.q = q;
   a.pool_k = pool_k;
   a.pool_v = pool_v;
@@ -463,6 +485,20 @@ sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, b
   a.kv_fp8 = kv_fp8;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  return SGL_OK;
+}
+
+sgl_status decode_entry(const void* q, const void* pool_k, const void* pool_v, bool kv_fp8,
+                        float k_scale, float v_scale, const int32_t* req_to_token, int32_t rtt_rows,
+                        int32_t rtt_stride, const int32_t* req_pool_idx, const int32_t* seq_lens,
+                        int32_t batch, int32_t max_seq_len, void* out, void* workspace,
+                        size_t workspace_bytes, const sgl_attn_dims* dims, sgl_stream_t stream) {
+  DecodeArgs a;
+  bool empty = false;
+  const sgl_status st = decode_args(q, pool_k, pool_v, kv_fp8, k_scale, v_scale, req_to_token, rtt_rows,
+                                    rtt_stride, req_pool_idx, seq_lens, batch, max_seq_len, out, workspace,
+                                    workspace_bytes, dims, &a, &empty);
+  if (st != SGL_OK || empty) return st;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 }  // namespace
@@ -662,6 +698,46 @@ sgl_status sgl_check_decode_indices(const int32_t* req_to_token, int32_t rtt_row
                                                     seq_lens, nullptr, 1, pool_size, max_seq_len, 0,
                                                     d_error);
   return last_launch();
+}
+
+sgl_status sgl_mixed_attention(
+    const void* q_ext, const void* k_new, const void* v_new, const int32_t* ext_req_pool_idx,
+    const int32_t* prefix_lens, const int32_t* extend_lens, int32_t ext_batch, int32_t total_extend,
+    int32_t max_extend, int32_t max_prefix, void* out_ext, void* ext_workspace, size_t ext_workspace_bytes,
+    const void* q_dec, const int32_t* dec_req_pool_idx, const int32_t* seq_lens, int32_t dec_batch,
+    int32_t max_seq_len, void* out_dec, void* dec_workspace, size_t dec_workspace_bytes, const void* pool_k,
+    const void* pool_v, const int32_t* req_to_token, int32_t rtt_rows, int32_t rtt_stride, int32_t extend_sms,
+    const sgl_attn_dims* dims, sgl_stream_t stream) {
+  ExtendArgs ea;
+  DecodeArgs da;
+  bool e_empty = true, d_empty = true;
+  sgl_status st = extend_args(q_ext, k_new, v_new, pool_k, pool_v, false, 1.f, 1.f, req_to_token, rtt_rows,
+                              rtt_stride, ext_req_pool_idx, prefix_lens, extend_lens, ext_batch, total_extend,
+                              max_extend, max_prefix, out_ext, ext_workspace, ext_workspace_bytes, dims, &ea,
+                              &e_empty);
+  if (st != SGL_OK) return st;
+  st = decode_args(q_dec, pool_k, pool_v, false, 1.f, 1.f, req_to_token, rtt_rows, rtt_stride,
+                   dec_req_pool_idx, seq_lens, dec_batch, max_seq_len, out_dec, dec_workspace,
+                   dec_workspace_bytes, dims, &da, &d_empty);
+  if (st != SGL_OK) return st;
+  if (e_empty) ea.batch = 0;
+  if (d_empty) da.batch = 0;
+  if (extend_sms < 0) return SGL_ERR_INVALID_ARG;
+  if (extend_sms == 0 && !e_empty && !d_empty) {
+    // split the SMs by an estimate of each side's time from the host values
+    // (mean lengths taken as half the maxima): extend flops at ~1.2 PFLOP/s,
+    // decode bytes at ~6.7 TB/s; CTAs whose side finishes first take the
+    // other side's work, so the estimate only sets where both start
+    const double te = 4.0 * dims->head_dim * dims->num_q_heads * (double)total_extend *
+                      (0.5 * max_prefix + 0.5 * max_extend) / 1.2e15;
+    const double td = (double)dec_batch * 0.5 * max_seq_len *
+                      (4.0 * dims->num_kv_heads * dims->head_dim + 4.0) / 6.7e12;
+    const int n = num_sms();
+    extend_sms = (int32_t)(n * te / (te + td) + 0.5);
+    if (extend_sms < 1) extend_sms = 1;
+    if (extend_sms > n - 1) extend_sms = n - 1;
+  }
+  return launch_mixed(ea, da, extend_sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,918 +1,14 @@
-// Paged decode attention: one query per request over all of its slots.
-//
-// "Inside SGLang", Step 3 (Prefill and decode have different shapes): a
-// decode step reads the key and value of every earlier token, so it is bound
-// by memory bandwidth; (Paged KV and the kernels that read it): the kernel
-// reads the request's slot indices from req_to_token and gathers its keys and
-// values from wherever they sit in the pool.
-//
-// Schedule (split-KV):
-//   1. plan    -- one block lists the work items (request, split): a
-//                 request's keys are cut into ceil(seq_len / 1024) runs of
-//                 near-equal length;
-//   2. split   -- a persistent grid (x: one wave of CTAs taking items from a
-//                 per-KV-head counter; y: KV head) runs
-//                 each item: the slot indices go to shared memory, K and V
-//                 rows of the KV head are gathered by 16-byte cp.async into a
-//                 ring of tiles (CUDA-core path: 6 stages of 16 bf16 / 32 e4m3
-//                 keys; tensor-core path: 4 stages of 32 / 64), and
-//                 the query heads of the group share every loaded row.  Each
-//                 warp takes a quarter of a tile: with one or two query heads
-//                 per KV head on CUDA cores (LPT = 8 or 16 lanes own one key,
-//                 each lane a slice of the head dim, every lane group an fp32
-//                 online-softmax state), with four or more on tensor cores
-//                 (warp-level MMAs whose rows are the query heads).  The
-//                 warps' states are merged at the end of the item.  Requests
-//                 with one split write the output directly; others write
-//                 their partial state;
-//   3. combine -- one warp per (request, query head) merges the partial
-//                 states of multi-split requests (max-rescaled sums).
-// Cascade decode (shared prefixes read once per group) runs the same three
-// kernels with a group pass before the split: the plan kernel derives each
-// request's shared length and group count from the groups, the split kernel
-// covers only the private tail [shared_len, seq_len), and the combine merges
-// the group states (written by the tensor-core group kernel) with the tail's.
-// Scores are kept in the log2 domain (scale * log2(e) folded into q) and the
-// running max is only moved when a score exceeds it by more than 2^8, which
-// keeps every exponentiated weight <= 256 in fp32 and makes rescaling rare.
-#include <cuda_fp8.h>
-
-#include <type_traits>
-
-#include "common.cuh"
+// Launchers of the decode kernels (decode_dev.cuh): the workspace layout,
+// shape checks, the plan / split / combine launches and the cascade's group
+// pass before the split.
+#include "decode_dev.cuh"
 #include "launch.h"
 
 namespace sgl {
 
+using namespace dec;
+
 namespace {
-
-constexpr int kChunk = 1024;   // keys per work item
-constexpr int kTileBf16 = 32;  // tensor-core path: bf16 keys per pipeline stage (twice as many e4m3)
-constexpr int kStages = 4;     // tensor-core path: ring depth
-// the CUDA-core path (measured best there: a deeper ring of smaller tiles)
-constexpr int kTileBf16Fma = 16;
-constexpr int kStagesFma = 6;
-// resident split CTAs an SM on the tensor-core path (4 stages at 3 CTAs
-// measured against 3 stages at 4: within 0.5% on most workloads)
-constexpr int kMmaMinBlocks = 3;
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-
-struct Ws {
-  int32_t* item_start;  // [B+1]
-  int2* items;          // [max_items]
-  int32_t* n_items;     // [1]
-  int32_t* next_item;   // [Hkv] work counters (zeroed by the plan kernel)
-  int2* req_info;       // [B] (shared_len, number of groups); cascade only, else null
-  float2* part_ml;      // [max_items + B*max_depth, Hkv, G]  (max in log2 units, sum)
-  float* part_acc;      // [max_items + B*max_depth, Hkv, G, D]
-};
-
-// The groups of a cascade decode (all null / 0 for plain decode).
-struct Groups {
-  const int32_t* start;
-  const int32_t* len;
-  const int32_t* depth;
-  const int32_t* member_off;
-  const int32_t* members;
-  int32_t n_groups, max_depth;
-};
-
-__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-inline int64_t max_items_for(int32_t batch, int32_t max_seq_len) {
-  return (int64_t)batch * ((max_seq_len + kChunk - 1) / kChunk);
-}
-
-// partial-state entries: the split items, then (cascade) B x max_depth group states
-inline size_t ws_layout(int32_t batch, int64_t max_items, int32_t Hkv, int32_t G, int32_t D,
-                        int32_t max_depth, bool cascade, void* base, Ws* ws) {
-  const int64_t n_part = max_items + (cascade ? (int64_t)batch * max_depth : 0);
-  size_t off = 0;
-  size_t o_start = off;
-  off = align256(off + sizeof(int32_t) * (size_t)(batch + 1));
-  size_t o_items = off;
-  off = align256(off + sizeof(int2) * (size_t)max_items);
-  size_t o_n = off;
-  off = align256(off + sizeof(int32_t));
-  size_t o_next = off;
-  off = align256(off + sizeof(int32_t) * (size_t)Hkv);
-  size_t o_info = off;
-  if (cascade) off = align256(off + sizeof(int2) * (size_t)batch);
-  size_t o_ml = off;
-  off = align256(off + sizeof(float2) * (size_t)n_part * Hkv * G);
-  size_t o_acc = off;
-  off = align256(off + sizeof(float) * (size_t)n_part * Hkv * G * D);
-  if (ws && base) {
-    char* b = static_cast<char*>(base);
-    ws->item_start = reinterpret_cast<int32_t*>(b + o_start);
-    ws->items = reinterpret_cast<int2*>(b + o_items);
-    ws->n_items = reinterpret_cast<int32_t*>(b + o_n);
-    ws->next_item = reinterpret_cast<int32_t*>(b + o_next);
-    ws->req_info = cascade ? reinterpret_cast<int2*>(b + o_info) : nullptr;
-    ws->part_ml = reinterpret_cast<float2*>(b + o_ml);
-    ws->part_acc = reinterpret_cast<float*>(b + o_acc);
-  }
-  return off;
-}
-
-struct Params {
-  const __nv_bfloat16* q;
-  const uint8_t* pool_k;  // [S, Hkv, D] rows of bf16 or e4m3 values
-  const uint8_t* pool_v;
-  const int32_t* req_to_token;
-  int64_t rtt_stride;
-  const int32_t* req_pool_idx;
-  const int32_t* seq_lens;
-  __nv_bfloat16* out;
-  // Hkv: KV heads as the kernels see them.  A group of more than 16 query
-  // heads per KV head runs as kv_split "virtual" KV heads of Hq / Hkv query
-  // heads each (virtual head v reads pool head v / kv_split; query heads,
-  // outputs and partial states keep the same flat order); Hkv_pool is the
-  // pool's own KV head count (the row stride of a slot).
-  int32_t batch, Hq, Hkv;
-  int32_t kv_split, Hkv_pool;
-  float scale_log2;  // softmax scale * log2(e) * K scale (1 for a bf16 pool)
-  float v_scale;     // V scale of an e4m3 pool (1 for bf16), applied to the output
-  Ws ws;
-  int64_t group_base;  // first partial entry of the group states (= max_items)
-  int32_t max_depth;   // group states per request (cascade), else 0
-};
-
-// ---------------------------------------------------------------- plan
-
-__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __restrict__ seq_lens,
-                                                           int32_t batch, int64_t max_items,
-                                                           int32_t Hkv, Ws ws, Groups gr) {
-  __shared__ int32_t warp_tot[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int h = tid; h < Hkv; h += blockDim.x) ws.next_item[h] = 0;
-  if (ws.req_info != nullptr) {
-    // cascade: every membership raises its request's shared length to the
-    // group's end and its group count to the group's depth + 1
-    for (int r = tid; r < batch; r += blockDim.x) ws.req_info[r] = make_int2(0, 0);
-    __syncthreads();
-    for (int j = warp; j < gr.n_groups; j += blockDim.x >> 5) {
-      const int32_t a = gr.member_off[j], b = gr.member_off[j + 1];
-      const int32_t end = gr.start[j] + gr.len[j], cnt = gr.depth[j] + 1;
-      for (int32_t k = a + lane; k < b; k += 32) {
-        const int32_t r = gr.members[k];
-        if (r >= 0 && r < batch) {
-          atomicMax(&ws.req_info[r].x, end);
-          atomicMax(&ws.req_info[r].y, min(cnt, gr.max_depth));
-        }
-      }
-    }
-    __syncthreads();
-  }
-  // keys of request r handled by split items: the private tail [shared_len, seq_len)
-  auto tail_len = [&](int r) {
-    const int32_t sh = ws.req_info != nullptr ? __ldcg(&ws.req_info[r].x) : 0;
-    return max(seq_lens[r] - sh, 0);
-  };
-  const int per = (batch + blockDim.x - 1) / blockDim.x;
-  const int r0 = min(batch, tid * per), r1 = min(batch, r0 + per);
-  int32_t local = 0;
-  for (int r = r0; r < r1; ++r) local += (tail_len(r) + kChunk - 1) / kChunk;
-  // block-wide exclusive scan of `local`
-  int32_t inc = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int32_t t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int32_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    warp_tot[lane] = t;  // inclusive over warps
-  }
-  __syncthreads();
-  int32_t base = inc - local + (warp > 0 ? warp_tot[warp - 1] : 0);
-  for (int r = r0; r < r1; ++r) {
-    ws.item_start[r] = base;
-    const int32_t ns = (tail_len(r) + kChunk - 1) / kChunk;
-    for (int32_t s = 0; s < ns; ++s)
-      if (base + s < max_items) ws.items[base + s] = make_int2(r, s);
-    base += ns;
-  }
-  if (tid == blockDim.x - 1) {
-    ws.item_start[batch] = base;
-    *ws.n_items = (int32_t)min((int64_t)base, max_items);
-  }
-}
-
-// ---------------------------------------------------------------- split
-
-// LPT lanes own one key; each lane holds D/LPT elements of the head dim, in
-// chunks of at most 16 bytes of the stored row (8 bf16 or 16 e4m3 values);
-// the LPT lanes' chunks are contiguous, so a warp's loads are coalesced.
-// LPT = 8 for small head groups, 16 when G*D is large (keeps the per-lane
-// query and accumulator registers bounded).  KV is the pool's element type:
-// __nv_bfloat16, or uint8_t holding e4m3 codes.
-template <int D, int LPT, typename KV>
-struct Lane {
-  static constexpr int kBytes = (int)sizeof(KV);
-  static constexpr int kRowBytes = D * kBytes;
-  static constexpr int kRowVecs = kRowBytes / 16;  // 16-byte vectors per row
-  static constexpr int kElems = D / LPT;           // elements per lane
-  static constexpr int kChunkElems = (16 / kBytes) < kElems ? (16 / kBytes) : kElems;
-  static constexpr int kChunks = kElems / kChunkElems;
-  static constexpr int kGroups = 32 / LPT;         // keys per warp instruction
-  // element offset of chunk c of lane li
-  static __device__ __forceinline__ int elem(int c, int li) {
-    return c * (kChunkElems * LPT) + li * kChunkElems;
-  }
-};
-
-// n stored values of type KV at p -> n floats (e4m3 codes are exact in float)
-template <typename KV, int N>
-SGL_DEV void load_row_chunk(const uint8_t* p, float* f) {
-  if constexpr (sizeof(KV) == 2) {
-    static_assert(N == 8, "one 16-byte vector of bf16");
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(p), f);
-  } else {
-    static_assert(N == 8 || N == 16, "8 or 16 e4m3 codes");
-    uint32_t w[N / 4];
-    if constexpr (N == 16) {
-      const uint4 v = *reinterpret_cast<const uint4*>(p);
-      w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
-    } else {
-      const uint2 v = *reinterpret_cast<const uint2*>(p);
-      w[0] = v.x, w[1] = v.y;
-    }
-#pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
-            (__nv_fp8x2_storage_t)(w[i] >> (16 * h)), __NV_E4M3);
-        const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&r));
-        f[4 * i + 2 * h] = x.x;
-        f[4 * i + 2 * h + 1] = x.y;
-      }
-    }
-  }
-}
-
-template <int D, int G, int LPT>
-__host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 3 : 2; }
-
-// Which (pool type, group size) take the tensor-core path (measured best):
-// three or more query heads per KV head, or two or more on an e4m3 pool.
-// With one or two bf16 query heads per KV head the 16-row MMAs carry 14-15
-// empty rows and the CUDA-core path is faster (7-8%); from four heads on the
-// MMAs remove most of the per-key instructions (tree decode 23% faster at
-// G = 4); above 8 heads the MMA rows 8..15 carry heads too.  e4m3 operands of
-// the tensor-core path are widened by bit placement on the integer pipe
-// (code * 2^-8 as f16, the 2^8 folded back into the scores and the published
-// sums; the hardware e4m3x2 -> f16x2 conversion measured the same).
-constexpr int kFp8MmaMinG = 2;
-template <typename KV, int G>
-__host__ __device__ constexpr bool use_mma() {
-  return G >= 3 || (sizeof(KV) == 1 && G >= kFp8MmaMinG);
-}
-
-// Per-warp attention state of the CUDA-core path: LPT lanes own one key, each
-// lane a slice of the head dim; every lane group keeps an fp32 online-softmax
-// state (max, sum, weighted V sum) for each of the G query heads.
-template <int D, int G, int LPT, typename KV, int kTile>
-struct FmaState {
-  using L = Lane<D, LPT, KV>;
-  static constexpr int EL = L::kElems, CE = L::kChunkElems;
-  float qf[G][EL];
-  float m[G], l[G], acc[G][EL];
-  int grp, li, warp;
-
-  SGL_DEV void init(int lane, int w) {
-    grp = lane / LPT;
-    li = lane % LPT;
-    warp = w;
-  }
-  // this lane's slice of the G query heads, pre-scaled into log2 units
-  SGL_DEV void load_q(const __nv_bfloat16* qb, float scale_log2) {
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int c = 0; c < L::kChunks; ++c)
-#pragma unroll
-        for (int u = 0; u < CE; u += 8) {
-          uint4 raw = *reinterpret_cast<const uint4*>(qb + h * D + L::elem(c, li) + u);
-          bf16x8_to_f32(raw, &qf[h][c * CE + u]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) qf[h][c * CE + u + e] *= scale_log2;
-        }
-  }
-  SGL_DEV void reset() {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EL; ++e) acc[h][e] = 0.f;
-    }
-  }
-  // the stage's keys key0 .. key0 + kTile (those < n are valid)
-  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float) {
-#pragma unroll
-    for (int sub = 0; sub < kTile / (L::kGroups * kWarps); ++sub) {
-      const int tok = warp * (kTile / kWarps) + sub * L::kGroups + grp;
-      const bool valid = key0 + tok < n;
-      float kf[EL];
-#pragma unroll
-      for (int c = 0; c < L::kChunks; ++c)
-        load_row_chunk<KV, CE>(ks + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &kf[c * CE]);
-      // q.k and p.v on the packed fp32 pipe (two lanes of FMA per instruction)
-      float s[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < EL; e += 2)
-          a = ffma2(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), a);
-        s[h] = a.x + a.y;
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int o = 1; o < LPT; o <<= 1) s[h] += __shfl_xor_sync(0xffffffffu, s[h], o);
-        if (!valid) s[h] = -INFINITY;
-      }
-      bool need = false;
-#pragma unroll
-      for (int h = 0; h < G; ++h) need |= s[h] > m[h] + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          if (s[h] > m[h] + kRescaleThreshold) {
-            const float a = ex2(m[h] - s[h]);
-            m[h] = s[h];
-            l[h] *= a;
-#pragma unroll
-            for (int e = 0; e < EL; ++e) acc[h][e] *= a;
-          }
-        }
-      }
-      float vf[EL];
-#pragma unroll
-      for (int c = 0; c < L::kChunks; ++c)
-        load_row_chunk<KV, CE>(vs + tok * L::kRowBytes + L::kBytes * L::elem(c, li), &vf[c * CE]);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pw = valid ? ex2(s[h] - m[h]) : 0.f;
-        l[h] += pw;
-#pragma unroll
-        for (int e = 0; e < EL; e += 2) {
-          const float2 a = ffma2(make_float2(pw, pw), make_float2(vf[e], vf[e + 1]),
-                                 make_float2(acc[h][e], acc[h][e + 1]));
-          acc[h][e] = a.x;
-          acc[h][e + 1] = a.y;
-        }
-      }
-    }
-  }
-  // merge the warp's lane groups and write its state to the CTA scratch
-  SGL_DEV void publish(float* red_acc, float* red_m, float* red_l) {
-#pragma unroll
-    for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
-        const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
-        const float mn = fmaxf(m[h], mo);
-        const float fa = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
-        const float fb = mo == -INFINITY ? 0.f : ex2(mo - mn);
-        l[h] = l[h] * fa + lo * fb;
-#pragma unroll
-        for (int e = 0; e < EL; ++e) {
-          const float ao = __shfl_xor_sync(0xffffffffu, acc[h][e], off);
-          acc[h][e] = acc[h][e] * fa + ao * fb;
-        }
-        m[h] = mn;
-      }
-    }
-    if (grp == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-#pragma unroll
-          for (int e = 0; e < CE; ++e)
-            red_acc[(warp * G + h) * D + L::elem(c, li) + e] = acc[h][c * CE + e];
-        if (li == 0) {
-          red_m[warp * G + h] = m[h];
-          red_l[warp * G + h] = l[h];
-        }
-      }
-    }
-  }
-};
-
-// Per-warp attention state of the tensor-core path: the G query heads are the
-// rows of warp-level MMAs (m16n8k16 / m16n8k8, rows G..15 zero), lane (g, t)
-// = (lane / 4, lane % 4).  q.k contracts over the head dim in an order both
-// operands share (lane t holds dims [t*D/4, (t+1)*D/4) of its row, four per
-// k-step), so each lane's K row slice is one run of 16-byte loads; p.v
-// permutes the output columns so that lane g's V loads are contiguous (n-col
-// g of 8-column block j of 32-column block sb is dim 32*sb + 4*g + j; lane
-// (g, t) ends up holding dims 32*sb + 8*t .. +7 of head g).  bf16 pools use
-// bf16 operands; e4m3 pools convert codes to f16 operands two at a time.
-// Accumulation and the online softmax stay fp32; P is rounded to the operand
-// type before the p.v product.
-template <int D, int G, typename KV, int kTile>
-struct MmaState {
-  static constexpr int kBytes = (int)sizeof(KV);
-  static constexpr int kRowBytes = D * kBytes;
-  static constexpr int KS = D / 16;          // k-steps of q.k
-  static constexpr int SB = D / 32;          // 32-column blocks of p.v
-  static constexpr int KW = kTile / kWarps;  // keys of a warp per stage: 8 bf16, 16 e4m3
-  static constexpr int DL = D / 4;           // head-dim values of one lane in q.k
-  static constexpr bool kTwoRows = G > 8;    // rows 8..15 carry heads too
-  static constexpr int NR = kTwoRows ? 2 : 1;  // rows of a lane: g (and g + 8)
-  static_assert(G <= 16, "at most 16 query heads per KV head");
-  static_assert(KW == (kBytes == 2 ? 8 : 16), "stage shape");
-  // e4m3 pools with 1, 2 or 4 query heads per KV head: the K codes go to the
-  // tensor core as they are (m16n8k32 e4m3 MMAs, no widening), and the A
-  // rows hold each head's query as three e4m3 terms (hi + mid + lo: ~12
-  // significant bits, the head scaled by a power of two into e4m3's range),
-  // term j of head h in row j * G + h, so one MMA computes all three.  Lane
-  // g's rows are g and g + 8: with G <= 2 head g's terms are the rows g, g +
-  // G, g + 2G of lanes 4G and 8G on (two shuffles add them); with G = 4 they
-  // are rows g and g + 8 of the lane itself and row g + 4 of the lane 16 on.
-  static constexpr bool kDirectK = kBytes == 1 && (G <= 2 || G == 4);
-  static constexpr int KS8 = D / 32;         // k-steps of the e4m3 q.k
-  uint32_t qa[KS][2 * NR];  // per k-step: row g lo, row g hi (, row g+8 lo, row g+8 hi)
-  uint32_t q8[KS8][4];      // direct K: a0..a3 of k-step ks (rows g, g + 8; k = 4t.., 16 + 4t..)
-  float qmul;               // direct K: 2^-e of head g (rows g < G)
-  float o[SB][4][4];        // c0, c1: row g; c2, c3: row g + 8
-  float m[NR], l[NR];
-  int g, t, warp;
-
-  SGL_DEV void init(int lane, int w) {
-    g = lane >> 2;
-    t = lane & 3;
-    warp = w;
-  }
-  SGL_DEV void load_q(const __nv_bfloat16* qb, float) {
-    if constexpr (kDirectK) {
-      load_q_terms(qb);
-      return;
-    }
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      const int row = g + 8 * rr;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) qa[ks][2 * rr] = qa[ks][2 * rr + 1] = 0u;
-      if (row < G) {
-        const uint4* src = reinterpret_cast<const uint4*>(qb + row * D + DL * t);
-#pragma unroll
-        for (int v = 0; v < DL / 8; ++v) {
-          const uint4 w = src[v];
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t x = ws[i];
-            if constexpr (kBytes == 1)
-              x = pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-            qa[(4 * v + i) / 2][2 * rr + (4 * v + i) % 2] = x;
-          }
-        }
-      }
-    }
-  }
-  // Row g = j * G + h (j < 3): term j of head h, over this lane's dims
-  // DL * t .. DL * t + DL - 1 (the same dims its K loads cover), in k-step
-  // order: k-step ks holds dims 8 ks .. 8 ks + 7 of the slice, four a word.
-  // The head's scale 2^e puts its largest |q| in [128, 256) (the four lanes of
-  // a row hold its four slices); hi = e4m3(q 2^e), mid = e4m3(q 2^e - hi),
-  // lo = e4m3(q 2^e - hi - mid), each difference exact in fp32.
-  SGL_DEV void load_q_terms(const __nv_bfloat16* qb) {
-    // rows g and g + 8 belong to the same head (G divides 8) as terms
-    // g / G and (g + 8) / G
-    const int h = g % G, term0 = g / G, term1 = (g + 8) / G;
-    const bool live = g < 3 * G;
-    float x[DL];
-    float amax = 0.f;
-#pragma unroll
-    for (int v = 0; v < DL / 8; ++v) {
-      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (live) raw = *reinterpret_cast<const uint4*>(qb + h * D + DL * t + 8 * v);
-      bf16x8_to_f32(raw, &x[8 * v]);
-    }
-#pragma unroll
-    for (int i = 0; i < DL; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    int e = 0;
-    if (amax > 0.f) e = min(126, max(-126, 7 - (((__float_as_int(amax) >> 23) & 0xff) - 127)));
-    const float sc = __int_as_float((e + 127) << 23);
-    qmul = __int_as_float((127 - e) << 23);
-#pragma unroll
-    for (int ks = 0; ks < KS8; ++ks)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-          const int d = 8 * ks + 4 * hf + i;
-          float2 v = make_float2(x[d] * sc, x[d + 1] * sc);
-          uint32_t c0 = 0u, c1 = 0u;
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const __nv_fp8x2_storage_t cj = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-            if (j == term0) c0 = (uint32_t)cj;
-            if (j == term1) c1 = (uint32_t)cj;
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(cj, __NV_E4M3);
-            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            v = make_float2(v.x - back.x, v.y - back.y);
-          }
-          w0 |= c0 << (8 * i);
-          w1 |= c1 << (8 * i);
-        }
-        q8[ks][2 * hf] = live ? w0 : 0u;                      // row g
-        q8[ks][2 * hf + 1] = live && term1 < 3 ? w1 : 0u;     // row g + 8
-      }
-  }
-  SGL_DEV void qk8(float (&d4)[4], int ks_, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
-        : "r"(q8[ks_][0]), "r"(q8[ks_][1]), "r"(q8[ks_][2]), "r"(q8[ks_][3]), "r"(b0), "r"(b1));
-  }
-  SGL_DEV void reset() {
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      m[rr] = -INFINITY;
-      l[rr] = 0.f;
-    }
-#pragma unroll
-    for (int b = 0; b < SB; ++b)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[b][j][c] = 0.f;
-  }
-  SGL_DEV void qk(float (&d4)[4], int ks_, uint32_t b0, uint32_t b1) {
-    uint32_t a1 = 0u, a3 = 0u;  // rows g + 8
-    if constexpr (kTwoRows) {
-      a1 = qa[ks_][2];
-      a3 = qa[ks_][3];
-    }
-    if constexpr (kBytes == 2) {
-      asm volatile(
-          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-          "{%8,%9}, {%0,%1,%2,%3};"
-          : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
-          : "r"(qa[ks_][0]), "r"(a1), "r"(qa[ks_][1]), "r"(a3), "r"(b0), "r"(b1));
-    } else {
-      asm volatile(
-          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-          "{%8,%9}, {%0,%1,%2,%3};"
-          : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
-          : "r"(qa[ks_][0]), "r"(a1), "r"(qa[ks_][1]), "r"(a3), "r"(b0), "r"(b1));
-    }
-  }
-  // widened e4m3 operands hold code * 2^-8
-  static constexpr float kWiden = kBytes == 1 ? 256.f : 1.f;
-  SGL_DEV static void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) { e4m3x4_to_f16x2_scaled(w, lo, hi); }
-  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2_in) {
-    // widened K codes hold code * 2^-8; the direct path's scores carry the
-    // head's 2^e
-    const float scale_log2 = scale_log2_in * (kDirectK ? qmul : kWiden);
-    // ---- S = q.k for this warp's KW keys, 8 at a time; sv[nb][row set][c]
-    float sv[KW / 8][NR][2];
-#pragma unroll
-    for (int nb = 0; nb < KW / 8; ++nb) {
-      const uint8_t* row = ks + (warp * KW + nb * 8 + g) * kRowBytes + DL * t * kBytes;
-      float d4[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (kDirectK) {
-#pragma unroll
-        for (int v = 0; v < DL / 16; ++v) {  // 16 codes = two e4m3 k-steps
-          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
-          qk8(d4, 2 * v, w.x, w.y);
-          qk8(d4, 2 * v + 1, w.z, w.w);
-        }
-        // add head g's three term rows (rows past the terms hold zeros; lanes
-        // of rows >= G hold no head)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if constexpr (G == 4)
-            d4[c] += __shfl_down_sync(0xffffffffu, d4[c], 16) + d4[c + 2];
-          else
-            d4[c] += __shfl_down_sync(0xffffffffu, d4[c], 4 * G) + __shfl_down_sync(0xffffffffu, d4[c], 8 * G);
-        }
-      } else if constexpr (kBytes == 2) {
-#pragma unroll
-        for (int v = 0; v < DL / 8; ++v) {  // 8 bf16 = two k-steps
-          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
-          qk(d4, 2 * v, w.x, w.y);
-          qk(d4, 2 * v + 1, w.z, w.w);
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < DL / 16; ++v) {  // 16 codes = four k-steps
-          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t lo, hi;
-            widen4(ws[i], lo, hi);
-            qk(d4, 4 * v + i, lo, hi);
-          }
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < NR; ++rr)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          sv[nb][rr][c] =
-              key0 + warp * KW + nb * 8 + 2 * t + c < n ? d4[2 * rr + c] * scale_log2 : -INFINITY;
-    }
-    // ---- online softmax of row g (and g + 8); the 4 lanes of a row agree on m
-    float pv[KW / 8][NR][2];
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nb = 0; nb < KW / 8; ++nb) mx = fmax3(mx, sv[nb][rr][0], sv[nb][rr][1]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      if (mx > m[rr] + kRescaleThreshold) {
-        const float a = m[rr] == -INFINITY ? 0.f : ex2(m[rr] - mx);
-        m[rr] = mx;
-        l[rr] *= a;
-#pragma unroll
-        for (int b = 0; b < SB; ++b)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            o[b][j][2 * rr] *= a;
-            o[b][j][2 * rr + 1] *= a;
-          }
-      }
-#pragma unroll
-      for (int nb = 0; nb < KW / 8; ++nb)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          pv[nb][rr][c] = sv[nb][rr][c] == -INFINITY ? 0.f : ex2(sv[nb][rr][c] - m[rr]);
-          l[rr] += pv[nb][rr][c];
-        }
-    }
-    // ---- O += P V
-    const uint8_t* r0 = vs + (warp * KW + 2 * t) * kRowBytes;  // key 2t of this warp's keys
-    if constexpr (kBytes == 2) {
-      const uint32_t a0 = pack_bf16x2(pv[0][0][0], pv[0][0][1]);
-      const uint32_t a1 = kTwoRows ? pack_bf16x2(pv[0][NR - 1][0], pv[0][NR - 1][1]) : 0u;
-#pragma unroll
-      for (int b = 0; b < SB; ++b) {
-        const uint2 x = *reinterpret_cast<const uint2*>(r0 + 2 * (32 * b + 4 * g));
-        const uint2 y = *reinterpret_cast<const uint2*>(r0 + kRowBytes + 2 * (32 * b + 4 * g));
-        const uint32_t bj[4] = {__byte_perm(x.x, y.x, 0x5410), __byte_perm(x.x, y.x, 0x7632),
-                                __byte_perm(x.y, y.y, 0x5410), __byte_perm(x.y, y.y, 0x7632)};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          asm volatile(
-              "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
-              "{%0,%1,%2,%3};"
-              : "+f"(o[b][j][0]), "+f"(o[b][j][1]), "+f"(o[b][j][2]), "+f"(o[b][j][3])
-              : "r"(a0), "r"(a1), "r"(bj[j]));
-      }
-    } else {
-      const uint32_t a0 = pack_f16x2(pv[0][0][0], pv[0][0][1]), a2 = pack_f16x2(pv[1][0][0], pv[1][0][1]);
-      const uint32_t a1 = kTwoRows ? pack_f16x2(pv[0][NR - 1][0], pv[0][NR - 1][1]) : 0u;
-      const uint32_t a3 = kTwoRows ? pack_f16x2(pv[1][NR - 1][0], pv[1][NR - 1][1]) : 0u;
-#pragma unroll
-      for (int b = 0; b < SB; ++b) {
-        const int col = 32 * b + 4 * g;
-        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(r0 + col);
-        const uint32_t x1 = *reinterpret_cast<const uint32_t*>(r0 + kRowBytes + col);
-        const uint32_t y0 = *reinterpret_cast<const uint32_t*>(r0 + 8 * kRowBytes + col);
-        const uint32_t y1 = *reinterpret_cast<const uint32_t*>(r0 + 9 * kRowBytes + col);
-        const uint32_t xa = __byte_perm(x0, x1, 0x5140), xb = __byte_perm(x0, x1, 0x7362);
-        const uint32_t ya = __byte_perm(y0, y1, 0x5140), yb = __byte_perm(y0, y1, 0x7362);
-        uint32_t b0[4], b1[4];
-        widen4(xa, b0[0], b0[1]);
-        widen4(xb, b0[2], b0[3]);
-        widen4(ya, b1[0], b1[1]);
-        widen4(yb, b1[2], b1[3]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          asm volatile(
-              "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-              "{%8,%9}, {%0,%1,%2,%3};"
-              : "+f"(o[b][j][0]), "+f"(o[b][j][1]), "+f"(o[b][j][2]), "+f"(o[b][j][3])
-              : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0[j]), "r"(b1[j]));
-      }
-    }
-  }
-  SGL_DEV void publish(float* red_acc, float* red_m, float* red_l) {
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      float ls = l[rr];
-      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-      const int row = g + 8 * rr;
-      if (row < G) {
-        float* dst = red_acc + (warp * G + row) * D + 8 * t;
-#pragma unroll
-        for (int b = 0; b < SB; ++b)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            dst[32 * b + j] = o[b][j][2 * rr] * kWiden;  // back to code units
-            dst[32 * b + 4 + j] = o[b][j][2 * rr + 1] * kWiden;
-          }
-        if (t == 0) {
-          red_m[warp * G + row] = m[rr];
-          red_l[warp * G + row] = ls;
-        }
-      }
-    }
-  }
-};
-
-template <int D, int G, int LPT, typename KV>
-__host__ __device__ constexpr int split_min_blocks() {
-  return use_mma<KV, G>() ? kMmaMinBlocks : min_blocks<D, G, LPT>();
-}
-
-// Ring shape of the split kernel: the tensor-core path takes 32 bf16 keys per
-// stage (8 per warp), the CUDA-core path its own tile and depth.  A stage
-// holds the same bytes for either pool type (twice as many e4m3 keys).
-template <typename KV, int G>
-struct SplitRing {
-  static constexpr bool kMma = use_mma<KV, G>();
-  static constexpr int kTileB = kMma ? kTileBf16 : kTileBf16Fma;  // bf16 keys per stage
-  static constexpr int kDepth = kMma ? kStages : kStagesFma;
-  static constexpr int kTile = kTileB * 2 / (int)sizeof(KV);            // keys per stage
-  template <int D>
-  static constexpr size_t bytes() { return (size_t)kDepth * 2 * kTileB * D * 2; }
-};
-
-template <int D, int G, int LPT, typename KV>
-__global__ void __launch_bounds__(kThreads, (split_min_blocks<D, G, LPT, KV>()))
-decode_split_kernel(Params p) {
-  using L = Lane<D, LPT, KV>;
-  using Ring = SplitRing<KV, G>;
-  constexpr int kTile = Ring::kTile;  // keys per pipeline stage
-  constexpr int kStages = Ring::kDepth;
-  constexpr int kTileBytes = kTile * L::kRowBytes;         // one K or V tile
-  constexpr int kStageBytes = 2 * kTileBytes;              // K then V
-  using State = std::conditional_t<use_mma<KV, G>(), MmaState<D, G, KV, kTile>,
-                                   FmaState<D, G, LPT, KV, kTile>>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  int32_t* s_slots = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
-  float* s_red = reinterpret_cast<float*>(smem);           // reuses the ring after an item
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int kvh = blockIdx.y;
-  const int32_t n_items = *p.ws.n_items;
-  const uint32_t ring = smem_u32(smem);
-  State st;
-  st.init(lane, warp);
-  // items are taken dynamically from the KV head's counter; the next index
-  // is fetched while the current item runs
-  __shared__ int32_t s_item[2];
-  if (tid == 0) s_item[0] = atomicAdd(&p.ws.next_item[kvh], 1);
-  __syncthreads();
-  int buf = 0;
-
-  for (int32_t item = s_item[0]; item < n_items; item = s_item[buf]) {
-    int32_t next = 0;
-    if (tid == 0) next = atomicAdd(&p.ws.next_item[kvh], 1);
-    const int2 it = p.ws.items[item];
-    const int r = it.x;
-    // the request's keys past its shared groups (all of them in plain decode)
-    // are cut into ceil(n / kChunk) near-equal items
-    const int2 info = p.ws.req_info != nullptr ? p.ws.req_info[r] : make_int2(0, 0);
-    const int32_t tail = max(p.seq_lens[r] - info.x, 0);
-    const int32_t ns = (tail + kChunk - 1) / kChunk;
-    const int32_t base = tail / ns, rem = tail % ns;
-    const int32_t t0 = info.x + it.y * base + min(it.y, rem);
-    const int32_t n = base + (it.y < rem ? 1 : 0);
-    const int32_t* rtt = p.req_to_token + (int64_t)p.req_pool_idx[r] * p.rtt_stride + t0;
-    for (int i = tid; i < n; i += kThreads) s_slots[i] = rtt[i];
-    st.load_q(p.q + ((int64_t)r * p.Hq + (int64_t)kvh * G) * D, p.scale_log2);
-    __syncthreads();  // slots visible; previous item's reduction scratch free
-
-    const int n_tiles = (n + kTile - 1) / kTile;
-    const uint8_t* kbase = p.pool_k + (int64_t)(kvh / p.kv_split) * L::kRowBytes;
-    const uint8_t* vbase = p.pool_v + (int64_t)(kvh / p.kv_split) * L::kRowBytes;
-    auto issue = [&](int tile, int stage) {
-      const uint32_t st_a = ring + stage * kStageBytes;
-      constexpr int kRowsPerPass = kThreads / L::kRowVecs;
-      const int vec = tid % L::kRowVecs;
-#pragma unroll
-      for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
-        const int tok = pass * kRowsPerPass + tid / L::kRowVecs;
-        const int32_t j = tile * kTile + tok;
-        const bool ok = j < n;
-        const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv_pool : 0;
-        const uint32_t d = st_a + tok * L::kRowBytes + vec * 16;
-        cp_async_16(d, kbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
-        cp_async_16(d + kTileBytes, vbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
-      }
-    };
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-      if (s < n_tiles) issue(s, s);
-      cp_async_commit();
-    }
-    st.reset();
-    for (int k = 0; k < n_tiles; ++k) {
-      cp_async_wait<kStages - 2>();
-      __syncthreads();
-      if (k + kStages - 1 < n_tiles) issue(k + kStages - 1, (k + kStages - 1) % kStages);
-      cp_async_commit();
-      const uint8_t* ks = smem + (k % kStages) * kStageBytes;
-      st.stage(ks, ks + kTileBytes, k * kTile, n, p.scale_log2);
-    }
-    cp_async_wait_all();
-
-    __syncthreads();  // every warp is done with the ring; reuse it for the reduction
-    // s_red layout: [warp][G][D] acc, then [warp][G] m, then [warp][G] l
-    float* red_acc = s_red;
-    float* red_m = s_red + kWarps * G * D;
-    float* red_l = red_m + kWarps * G;
-    st.publish(red_acc, red_m, red_l);
-    __syncthreads();
-    const bool single = ns == 1 && info.y == 0;
-    for (int idx = tid; idx < G * D; idx += kThreads) {
-      const int h = idx / D, d = idx % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * G + h]);
-      float Ls = 0.f, A = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = red_m[w * G + h];
-        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-        Ls += red_l[w * G + h] * f;
-        A += red_acc[(w * G + h) * D + d] * f;
-      }
-      if (single) {
-        p.out[((int64_t)r * p.Hq + (int64_t)kvh * G + h) * D + d] = __float2bfloat16_rn(A * (p.v_scale / Ls));
-      } else {
-        const int64_t slot = ((int64_t)item * p.Hkv + kvh) * G + h;
-        p.ws.part_acc[slot * D + d] = A;
-        if (d == 0) p.ws.part_ml[slot] = make_float2(M, Ls);
-      }
-    }
-    if (tid == 0) s_item[buf ^ 1] = next;
-    buf ^= 1;
-    __syncthreads();  // scratch, slots and the next item index
-  }
-}
-
-// ---------------------------------------------------------------- combine
-
-template <int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(Params p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (gw >= (int64_t)p.batch * p.Hq) return;
-  const int r = (int)(gw / p.Hq), h = (int)(gw % p.Hq);
-  const int32_t s0 = p.ws.item_start[r];
-  const int32_t n_split = p.ws.item_start[r + 1] - s0;
-  const int32_t n_grp = p.ws.req_info != nullptr ? p.ws.req_info[r].y : 0;
-  if (n_grp == 0 && n_split <= 1) return;     // a single split wrote the output
-  if (s0 + n_split > *p.ws.n_items) return;   // lengths above max_seq_len
-  const int32_t ns = n_grp + n_split;
-  const int G = p.Hq / p.Hkv;
-  const int kvh = h / G, hh = h % G;
-  // states in key order: the groups by depth, then the tail's splits
-  auto slot_of = [&](int32_t s) {
-    const int64_t e = s < n_grp ? p.group_base + (int64_t)r * p.max_depth + s : (int64_t)(s0 + s - n_grp);
-    return (e * p.Hkv + kvh) * G + hh;
-  };
-  float M = -INFINITY;
-  for (int32_t s = lane; s < ns; s += 32) M = fmaxf(M, p.ws.part_ml[slot_of(s)].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  constexpr int E = D / 32;
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float Ls = 0.f;
-  for (int32_t s = 0; s < ns; ++s) {
-    const int64_t sl = slot_of(s);
-    const float2 ml = p.ws.part_ml[sl];
-    const float f = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-    Ls += ml.y * f;
-    const float* a = p.ws.part_acc + sl * D;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(f, a[lane + 32 * e], acc[e]);
-  }
-  const float inv = p.v_scale / Ls;
-  __nv_bfloat16* o = p.out + ((int64_t)r * p.Hq + h) * D;
-#pragma unroll
-  for (int e = 0; e < E; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
-}
 
 template <int D, int G, typename KV>
 sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const GroupArgs* ga,
@@ -968,15 +64,6 @@ sgl_status run_g(int G, const Params& prm, int64_t max_items, const Groups& gr,
 
 }  // namespace
 
-// Split factor for groups of more than 16 query heads per KV head: the
-// smallest s dividing G with G / s <= 16 (1 for G <= 16).
-static int32_t kv_split_for(int32_t G) {
-  if (G <= 16) return 1;
-  for (int32_t s = 2; s <= G; ++s)
-    if (G % s == 0 && G / s <= 16) return s;
-  return G;
-}
-
 size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, int32_t Hkv,
                               int32_t D, bool cascade, int32_t max_depth) {
   const size_t head = cascade ? kCascadeStatusBytes : 0;
@@ -998,72 +85,14 @@ sgl_status decode_shape_supported(int32_t num_q_heads, int32_t num_kv_heads) {
 sgl_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.batch == 0) return SGL_OK;
   if (decode_shape_supported(a.num_q_heads, a.num_kv_heads) != SGL_OK) return SGL_ERR_UNSUPPORTED;
-  const int G_pool = a.num_q_heads / a.num_kv_heads;
-  const int split = kv_split_for(G_pool);
-  const int G = G_pool / split;                 // query heads of a (virtual) KV head
-  const int Hkv = a.num_kv_heads * split;       // KV heads as the kernels see them
-  const int64_t max_items = max_items_for(a.batch, a.max_seq_len);
   Params prm;
-  prm.q = static_cast<const __nv_bfloat16*>(a.q);
-  prm.pool_k = static_cast<const uint8_t*>(a.pool_k);
-  prm.pool_v = static_cast<const uint8_t*>(a.pool_v);
-  prm.req_to_token = a.req_to_token;
-  prm.rtt_stride = a.rtt_stride;
-  prm.req_pool_idx = a.req_pool_idx;
-  prm.seq_lens = a.seq_lens;
-  prm.out = static_cast<__nv_bfloat16*>(a.out);
-  prm.batch = a.batch;
-  prm.Hq = a.num_q_heads;
-  prm.Hkv = Hkv;
-  prm.kv_split = split;
-  prm.Hkv_pool = a.num_kv_heads;
-  // the K scale of an e4m3 pool folds into the query, the V scale into the output
-  prm.scale_log2 = a.sm_scale * 1.4426950408889634f * (a.kv_fp8 ? a.k_scale : 1.f);
-  prm.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
-  // cascade: word 0 of the workspace is the group pass's status; the decode
-  // scratch follows the status bytes
-  const size_t head = a.cascade ? kCascadeStatusBytes : 0;
-  const int32_t max_depth = a.cascade ? a.max_depth : 0;
-  char* base = static_cast<char*>(a.workspace);
-  if (base == nullptr) return SGL_ERR_WORKSPACE;
-  const size_t need = head + ws_layout(a.batch, max_items, Hkv, G, a.head_dim, max_depth,
-                                       a.cascade, base + head, &prm.ws);
-  if (a.workspace_bytes < need) return SGL_ERR_WORKSPACE;
-  prm.group_base = max_items;
-  prm.max_depth = max_depth;
-  Groups gr = {};
-  GroupArgs ga = {};
-  const bool groups = a.cascade && a.n_groups > 0;
-  if (groups) {
-    gr = Groups{a.group_start, a.group_len, a.group_depth, a.group_member_off, a.group_members,
-                a.n_groups, max_depth};
-    ga.q = a.q;
-    ga.pool_k = a.pool_k;
-    ga.pool_v = a.pool_v;
-    ga.req_to_token = a.req_to_token;
-    ga.rtt_stride = a.rtt_stride;
-    ga.req_pool_idx = a.req_pool_idx;
-    ga.group_start = a.group_start;
-    ga.group_len = a.group_len;
-    ga.group_depth = a.group_depth;
-    ga.member_off = a.group_member_off;
-    ga.members = a.group_members;
-    ga.batch = a.batch;
-    ga.n_groups = a.n_groups;
-    ga.max_members = a.max_group_members;
-    ga.max_depth = max_depth;
-    ga.part_ml = prm.ws.part_ml;
-    ga.part_acc = prm.ws.part_acc;
-    ga.part_base = max_items;
-    ga.status = reinterpret_cast<int*>(base);
-    ga.num_q_heads = a.num_q_heads;
-    ga.num_kv_heads = a.num_kv_heads;
-    ga.head_dim = a.head_dim;
-    ga.sm_scale = a.sm_scale;
-    ga.kv_fp8 = a.kv_fp8;
-    ga.k_scale = a.k_scale;
-  }
-  const GroupArgs* gp = groups ? &ga : nullptr;
+  DecodePlan pl;
+  const sgl_status st = make_decode_params(a, &prm, &pl);
+  if (st != SGL_OK) return st;
+  const int G = pl.G;
+  const int64_t max_items = pl.max_items;
+  const Groups& gr = pl.gr;
+  const GroupArgs* gp = pl.groups ? &pl.ga : nullptr;
   if (a.kv_fp8) {
     if (a.head_dim == 128) return run_g<128, uint8_t>(G, prm, max_items, gr, gp, stream);
     if (a.head_dim == 64) return run_g<64, uint8_t>(G, prm, max_items, gr, gp, stream);

@@ -148,4 +148,12 @@ struct ExtendArgs {
 size_t extend_workspace_bytes();
 sgl_status launch_extend(const ExtendArgs& a, cudaStream_t stream);
 
+// One launch for an extend batch and a plain decode batch over the same bf16
+// pools (mixed.cu): persistent CTAs, one an SM, the first extend_ctas taking
+// extend tiles first and the rest decode work first.  Shapes the single launch
+// is not built for (mixed_launch_built false) run the two kernels in turn.
+// Words 1..3 of the extend workspace hold the launch's work counters.
+bool mixed_launch_built(const ExtendArgs& e, const DecodeArgs& d);
+sgl_status launch_mixed(const ExtendArgs& e, const DecodeArgs& d, int32_t extend_ctas, cudaStream_t stream);
+
 }  // namespace sgl

@@ -129,3 +129,23 @@ def test_cascade_group_pass_gives_up_then_recovers():
     torch.cuda.synchronize()
     assert _status(ws2) == 0
     assert_close(W.bf16_bits(out), oracle_decode(w, 0), "cascade after a timed-out call")
+
+
+def test_mixed_launch_gives_up_then_recovers():
+    """The single mixed launch: its extend tiles' waits give up (the CTA that
+    ran one takes no more work), the decode work still completes, and the next
+    call with the default limit equals the separate calls."""
+    from test_gpu_mixed import _store_step, mixed, separate
+    w = W.chunked_prefill_mix(pool_size=1 << 19, n_decode=24)
+    run = Run(w)
+    _store_step(run)
+    ref_e, ref_d = separate(run)
+    ws = B.new_workspace(256, DEV)
+    with short_waits():
+        mixed(run, 60, ws)
+    assert _status(ws) == TIMEOUT_CODE
+    _device_answers()
+    ws2 = B.new_workspace(256, DEV)
+    got_e, got_d = mixed(run, 60, ws2)
+    assert _status(ws2) == 0
+    assert np.array_equal(got_e, ref_e) and np.array_equal(got_d, ref_d)
