@@ -54,10 +54,17 @@ def peaks():
 
 
 def kernel_source_hash(name: str) -> str:
+    """Hash of a kernel's sources: common.cuh, the launcher file and, where
+    there is one, the device header beside it (decode.cu -> decode_dev.cuh)."""
     import hashlib
+    csrc = os.path.join(ROOT, "radixattention_prefix_shared_gb300", "csrc")
+    files = ["common.cuh", name]
+    dev = name[:-3] + "_dev.cuh" if name.endswith(".cu") else None
+    if dev is not None and os.path.exists(os.path.join(csrc, dev)):
+        files.append(dev)
     h = hashlib.sha256()
-    for f in ("common.cuh", name):
-        with open(os.path.join(ROOT, "radixattention_prefix_shared_gb300", "csrc", f), "rb") as fh:
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
