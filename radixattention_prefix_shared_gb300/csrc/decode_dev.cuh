@@ -57,6 +57,12 @@ constexpr int kStagesFma = 6;
 // resident split CTAs an SM on the tensor-core path (4 stages at 3 CTAs
 // measured against 3 stages at 4: within 0.5% on most workloads)
 constexpr int kMmaMinBlocks = 3;
+// the e4m3 path with both products on the tensor core (E4m3MmaState): 3
+// stages at 4 CTAs an SM (128 registers); measured against 4 stages at 3
+// CTAs (160 registers): chunked-mix e4m3 decode 5,322 against 5,235 GB/s
+// (and at one head per KV head 4,550 against 3,210)
+constexpr int kStagesE4m3 = 3;
+constexpr int kE4m3MinBlocks = 4;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -276,14 +282,22 @@ __host__ __device__ constexpr int min_blocks() { return 2 * G * D / LPT <= 64 ? 
 // With one or two bf16 query heads per KV head the 16-row MMAs carry 14-15
 // empty rows and the CUDA-core path is faster (7-8%); from four heads on the
 // MMAs remove most of the per-key instructions (tree decode 23% faster at
-// G = 4); above 8 heads the MMA rows 8..15 carry heads too.  e4m3 operands of
-// the tensor-core path are widened by bit placement on the integer pipe
-// (code * 2^-8 as f16, the 2^8 folded back into the scores and the published
-// sums; the hardware e4m3x2 -> f16x2 conversion measured the same).
-constexpr int kFp8MmaMinG = 2;
+// G = 4); above 8 heads the MMA rows 8..15 carry heads too.  On e4m3 pools
+// with 2 or 4 heads both products take the codes as they are (E4m3MmaState);
+// with other group sizes MmaState widens them by bit placement on the integer pipe (code
+// * 2^-8 as f16, the 2^8 folded back into the scores and the published sums;
+// the hardware e4m3x2 -> f16x2 conversion measured the same).
 template <typename KV, int G>
 __host__ __device__ constexpr bool use_mma() {
-  return G >= 3 || (sizeof(KV) == 1 && G >= kFp8MmaMinG);
+  return G >= 3 || (sizeof(KV) == 1 && G >= 2);
+}
+// e4m3 pools with 2 or 4 query heads per KV head: both products on e4m3
+// MMAs, no widening (E4m3MmaState).  With one head the CUDA-core path stays
+// (Llama-7B-like e4m3 decode 4,710 against 4,570 GB/s on this one: the MMAs
+// cost the same per key at any group size, the CUDA-core work halves)
+template <typename KV, int G>
+__host__ __device__ constexpr bool use_e4m3_mma() {
+  return sizeof(KV) == 1 && (G == 2 || G == 4);
 }
 
 // Per-warp attention state of the CUDA-core path: LPT lanes own one key, each
@@ -292,6 +306,7 @@ __host__ __device__ constexpr bool use_mma() {
 template <int D, int G, int LPT, typename KV, int kTile>
 struct FmaState {
   using L = Lane<D, LPT, KV>;
+  static constexpr int kSwizzle = 0;  // plain ring rows
   static constexpr int EL = L::kElems, CE = L::kChunkElems;
   float qf[G][EL];
   float m[G], l[G], acc[G][EL];
@@ -434,6 +449,7 @@ struct FmaState {
 // type before the p.v product.
 template <int D, int G, typename KV, int kTile>
 struct MmaState {
+  static constexpr int kSwizzle = 0;  // plain ring rows
   static constexpr int kBytes = (int)sizeof(KV);
   static constexpr int kRowBytes = D * kBytes;
   static constexpr int KS = D / 16;          // k-steps of q.k
@@ -444,19 +460,7 @@ struct MmaState {
   static constexpr int NR = kTwoRows ? 2 : 1;  // rows of a lane: g (and g + 8)
   static_assert(G <= 16, "at most 16 query heads per KV head");
   static_assert(KW == (kBytes == 2 ? 8 : 16), "stage shape");
-  // e4m3 pools with 1, 2 or 4 query heads per KV head: the K codes go to the
-  // tensor core as they are (m16n8k32 e4m3 MMAs, no widening), and the A
-  // rows hold each head's query as three e4m3 terms (hi + mid + lo: ~12
-  // significant bits, the head scaled by a power of two into e4m3's range),
-  // term j of head h in row j * G + h, so one MMA computes all three.  Lane
-  // g's rows are g and g + 8: with G <= 2 head g's terms are the rows g, g +
-  // G, g + 2G of lanes 4G and 8G on (two shuffles add them); with G = 4 they
-  // are rows g and g + 8 of the lane itself and row g + 4 of the lane 16 on.
-  static constexpr bool kDirectK = kBytes == 1 && (G <= 2 || G == 4);
-  static constexpr int KS8 = D / 32;         // k-steps of the e4m3 q.k
   uint32_t qa[KS][2 * NR];  // per k-step: row g lo, row g hi (, row g+8 lo, row g+8 hi)
-  uint32_t q8[KS8][4];      // direct K: a0..a3 of k-step ks (rows g, g + 8; k = 4t.., 16 + 4t..)
-  float qmul;               // direct K: 2^-e of head g (rows g < G)
   float o[SB][4][4];        // c0, c1: row g; c2, c3: row g + 8
   float m[NR], l[NR];
   int g, t, warp;
@@ -467,10 +471,6 @@ struct MmaState {
     warp = w;
   }
   SGL_DEV void load_q(const __nv_bfloat16* qb, float) {
-    if constexpr (kDirectK) {
-      load_q_terms(qb);
-      return;
-    }
 #pragma unroll
     for (int rr = 0; rr < NR; ++rr) {
       const int row = g + 8 * rr;
@@ -492,66 +492,6 @@ struct MmaState {
         }
       }
     }
-  }
-  // Row g = j * G + h (j < 3): term j of head h, over this lane's dims
-  // DL * t .. DL * t + DL - 1 (the same dims its K loads cover), in k-step
-  // order: k-step ks holds dims 8 ks .. 8 ks + 7 of the slice, four a word.
-  // The head's scale 2^e puts its largest |q| in [128, 256) (the four lanes of
-  // a row hold its four slices); hi = e4m3(q 2^e), mid = e4m3(q 2^e - hi),
-  // lo = e4m3(q 2^e - hi - mid), each difference exact in fp32.
-  SGL_DEV void load_q_terms(const __nv_bfloat16* qb) {
-    // rows g and g + 8 belong to the same head (G divides 8) as terms
-    // g / G and (g + 8) / G
-    const int h = g % G, term0 = g / G, term1 = (g + 8) / G;
-    const bool live = g < 3 * G;
-    float x[DL];
-    float amax = 0.f;
-#pragma unroll
-    for (int v = 0; v < DL / 8; ++v) {
-      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (live) raw = *reinterpret_cast<const uint4*>(qb + h * D + DL * t + 8 * v);
-      bf16x8_to_f32(raw, &x[8 * v]);
-    }
-#pragma unroll
-    for (int i = 0; i < DL; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    int e = 0;
-    if (amax > 0.f) e = min(126, max(-126, 7 - (((__float_as_int(amax) >> 23) & 0xff) - 127)));
-    const float sc = __int_as_float((e + 127) << 23);
-    qmul = __int_as_float((127 - e) << 23);
-#pragma unroll
-    for (int ks = 0; ks < KS8; ++ks)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-          const int d = 8 * ks + 4 * hf + i;
-          float2 v = make_float2(x[d] * sc, x[d + 1] * sc);
-          uint32_t c0 = 0u, c1 = 0u;
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            const __nv_fp8x2_storage_t cj = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-            if (j == term0) c0 = (uint32_t)cj;
-            if (j == term1) c1 = (uint32_t)cj;
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(cj, __NV_E4M3);
-            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            v = make_float2(v.x - back.x, v.y - back.y);
-          }
-          w0 |= c0 << (8 * i);
-          w1 |= c1 << (8 * i);
-        }
-        q8[ks][2 * hf] = live ? w0 : 0u;                      // row g
-        q8[ks][2 * hf + 1] = live && term1 < 3 ? w1 : 0u;     // row g + 8
-      }
-  }
-  SGL_DEV void qk8(float (&d4)[4], int ks_, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
-        : "r"(q8[ks_][0]), "r"(q8[ks_][1]), "r"(q8[ks_][2]), "r"(q8[ks_][3]), "r"(b0), "r"(b1));
   }
   SGL_DEV void reset() {
 #pragma unroll
@@ -590,32 +530,15 @@ struct MmaState {
   static constexpr float kWiden = kBytes == 1 ? 256.f : 1.f;
   SGL_DEV static void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) { e4m3x4_to_f16x2_scaled(w, lo, hi); }
   SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2_in) {
-    // widened K codes hold code * 2^-8; the direct path's scores carry the
-    // head's 2^e
-    const float scale_log2 = scale_log2_in * (kDirectK ? qmul : kWiden);
+    // widened K codes hold code * 2^-8
+    const float scale_log2 = scale_log2_in * kWiden;
     // ---- S = q.k for this warp's KW keys, 8 at a time; sv[nb][row set][c]
     float sv[KW / 8][NR][2];
 #pragma unroll
     for (int nb = 0; nb < KW / 8; ++nb) {
       const uint8_t* row = ks + (warp * KW + nb * 8 + g) * kRowBytes + DL * t * kBytes;
       float d4[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (kDirectK) {
-#pragma unroll
-        for (int v = 0; v < DL / 16; ++v) {  // 16 codes = two e4m3 k-steps
-          const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
-          qk8(d4, 2 * v, w.x, w.y);
-          qk8(d4, 2 * v + 1, w.z, w.w);
-        }
-        // add head g's three term rows (rows past the terms hold zeros; lanes
-        // of rows >= G hold no head)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if constexpr (G == 4)
-            d4[c] += __shfl_down_sync(0xffffffffu, d4[c], 16) + d4[c + 2];
-          else
-            d4[c] += __shfl_down_sync(0xffffffffu, d4[c], 4 * G) + __shfl_down_sync(0xffffffffu, d4[c], 8 * G);
-        }
-      } else if constexpr (kBytes == 2) {
+      if constexpr (kBytes == 2) {
 #pragma unroll
         for (int v = 0; v < DL / 8; ++v) {  // 8 bf16 = two k-steps
           const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * v);
@@ -743,9 +666,231 @@ struct MmaState {
   }
 };
 
+// Per-warp attention state over an e4m3 pool with 2 or 4 query heads per KV
+// head: both products on e4m3 tensor-core MMAs (m16n8k32, fp32
+// accumulation), no code widened.
+//
+// q.k: the A rows hold each head's query as three e4m3 terms (hi + mid + lo:
+// ~12 significant bits, the head scaled by a power of two into e4m3's
+// range), term j of head h in row j * G + h, so one MMA computes all three;
+// the B columns are keys.  Lane g's rows are g and g + 8: with G = 2 head g's
+// terms are the rows g, g + 2, g + 4 of lanes 8 and 16 on (two shuffles add
+// them); with G = 4 they are rows g and g + 8 of the lane itself and row
+// g + 4 of the lane 16 on.  The warp's 16 keys of a stage go
+// to the columns of two MMAs so that, after the sums, lane (h, t) holds head
+// h's scores of keys 4t .. 4t + 3: the keys its p.v operand needs.
+//
+// p.v: A = V^T (16 head dims x 32 keys) straight from the ring by the
+// transposing 8-bit ldmatrix, keys 16..31 zero (a warp has 16 keys a stage);
+// B = P as two e4m3 terms of x = 2^8 p, hi = e4m3(x) and lo = e4m3(x - hi)
+// (~8 significant bits, as a bf16 P), column j * G + h holding term j of head
+// h.  The reference max is exact (moved whenever a block raises it), so p <=
+// 1 and x <= 256 fits e4m3; x and the row sums carry 2^8 until the state is
+// published.
+//
+// The ring rows are XOR-swizzled by 16-byte chunk (chunk c of row r at c ^ (r
+// & kSwizzle)), so the 8-row phases of both products' loads hit distinct banks.
+template <int D, int G, int kTile>
+struct E4m3MmaState {
+  static constexpr int kRowBytes = D;
+  static constexpr int kSwizzle = D / 16 - 1;  // 16-byte chunks a row, less one
+  static constexpr int KW = kTile / kWarps;    // keys of a warp per stage
+  static constexpr int DL = D / 4;             // head dims of one lane in q.k
+  static constexpr int KS8 = D / 32;           // k-steps of q.k
+  static constexpr int DB = D / 16;            // 16-dim blocks of p.v
+  static_assert(KW == 16, "16 keys a warp per stage");
+  static_assert(G == 2 || G == 4, "group sizes of this path");
+  uint32_t q8[KS8][4];  // a0..a3 of k-step ks (rows g, g + 8; k = 4t.., 16 + 4t..)
+  float qmul;           // 2^-e of head g (rows g < G)
+  float c[DB][4];       // p.v: rows (dims) 16 b + g, 16 b + 8 + g; columns 2t, 2t + 1
+  float m, l;           // head g's reference max and row sum (lanes g < G)
+  int g, t, warp;
+
+  SGL_DEV void init(int lane, int w) {
+    g = lane >> 2;
+    t = lane & 3;
+    warp = w;
+  }
+  SGL_DEV void load_q(const __nv_bfloat16* qb, float) { load_q_terms(qb); }
+  // Row g = j * G + h (j < 3): term j of head h, over this lane's dims
+  // DL * t .. DL * t + DL - 1 (the same dims its K loads cover), in k-step
+  // order: k-step ks holds dims 8 ks .. 8 ks + 7 of the slice, four a word.
+  // The head's scale 2^e puts its largest |q| in [128, 256) (the four lanes of
+  // a row hold its four slices); hi = e4m3(q 2^e), mid = e4m3(q 2^e - hi),
+  // lo = e4m3(q 2^e - hi - mid), each difference exact in fp32.
+  SGL_DEV void load_q_terms(const __nv_bfloat16* qb) {
+    // rows g and g + 8 belong to the same head (G divides 8) as terms
+    // g / G and (g + 8) / G
+    const int h = g % G, term0 = g / G, term1 = (g + 8) / G;
+    const bool live = g < 3 * G;
+    float x[DL];
+    float amax = 0.f;
+#pragma unroll
+    for (int v = 0; v < DL / 8; ++v) {
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (live) raw = *reinterpret_cast<const uint4*>(qb + h * D + DL * t + 8 * v);
+      bf16x8_to_f32(raw, &x[8 * v]);
+    }
+#pragma unroll
+    for (int i = 0; i < DL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int e = 0;
+    if (amax > 0.f) e = min(126, max(-126, 7 - (((__float_as_int(amax) >> 23) & 0xff) - 127)));
+    const float sc = __int_as_float((e + 127) << 23);
+    qmul = __int_as_float((127 - e) << 23);
+#pragma unroll
+    for (int ks = 0; ks < KS8; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+          const int d = 8 * ks + 4 * hf + i;
+          float2 v = make_float2(x[d] * sc, x[d + 1] * sc);
+          uint32_t c0 = 0u, c1 = 0u;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const __nv_fp8x2_storage_t cj = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+            if (j == term0) c0 = (uint32_t)cj;
+            if (j == term1) c1 = (uint32_t)cj;
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(cj, __NV_E4M3);
+            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            v = make_float2(v.x - back.x, v.y - back.y);
+          }
+          w0 |= c0 << (8 * i);
+          w1 |= c1 << (8 * i);
+        }
+        q8[ks][2 * hf] = live ? w0 : 0u;                      // row g
+        q8[ks][2 * hf + 1] = live && term1 < 3 ? w1 : 0u;     // row g + 8
+      }
+  }
+  SGL_DEV void qk8(float (&d4)[4], int ks_, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d4[0]), "+f"(d4[1]), "+f"(d4[2]), "+f"(d4[3])
+        : "r"(q8[ks_][0]), "r"(q8[ks_][1]), "r"(q8[ks_][2]), "r"(q8[ks_][3]), "r"(b0), "r"(b1));
+  }
+  SGL_DEV void reset() {
+    m = -INFINITY;
+    l = 0.f;
+#pragma unroll
+    for (int b = 0; b < DB; ++b)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) c[b][k] = 0.f;
+  }
+  SGL_DEV void stage(const uint8_t* ks, const uint8_t* vs, int key0, int n, float scale_log2_in) {
+    const float scale_log2 = scale_log2_in * qmul;  // the scores carry the head's 2^e
+    // ---- S: column g of MMA nb is key 4 (g / 2) + 2 nb + g % 2 of the warp's
+    // 16, so lane (h, t) ends with head h's scores of keys 4t + 2 nb + cc
+    float s[2][2];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      const int r = warp * KW + 4 * (g >> 1) + 2 * nb + (g & 1);
+      const uint8_t* row = ks + r * kRowBytes;
+      float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int v = 0; v < DL / 16; ++v) {  // 16 codes = two k-steps
+        const int chunk = ((DL / 16) * t + v) ^ (r & kSwizzle);
+        const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * chunk);
+        qk8(d4, 2 * v, w.x, w.y);
+        qk8(d4, 2 * v + 1, w.z, w.w);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        if constexpr (G == 4)
+          d4[cc] += __shfl_down_sync(0xffffffffu, d4[cc], 16) + d4[cc + 2];
+        else
+          d4[cc] += __shfl_down_sync(0xffffffffu, d4[cc], 4 * G) + __shfl_down_sync(0xffffffffu, d4[cc], 8 * G);
+        s[nb][cc] = key0 + warp * KW + 4 * t + 2 * nb + cc < n ? d4[cc] * scale_log2 : -INFINITY;
+      }
+    }
+    // ---- online softmax of head g over its 16 keys (lanes g < G); the
+    // reference moves whenever the block max is above it
+    float mx = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (__any_sync(0xffffffffu, g < G && mx > m)) {
+      const float mn = fmaxf(m, mx);
+      const float a = m == -INFINITY ? 0.f : ex2(m - mn);
+      m = mn;
+      l *= a;
+      // accumulator columns 2t, 2t + 1 belong to heads 2t % G, (2t + 1) % G
+      const float a0 = __shfl_sync(0xffffffffu, a, 4 * ((2 * t) % G));
+      const float a1 = __shfl_sync(0xffffffffu, a, 4 * ((2 * t + 1) % G));
+#pragma unroll
+      for (int b = 0; b < DB; ++b) {
+        c[b][0] *= a0;
+        c[b][2] *= a0;
+        c[b][1] *= a1;
+        c[b][3] *= a1;
+      }
+    }
+    // ---- P terms of keys 4t .. 4t + 3, one byte a key
+    uint32_t hi = 0u, lo = 0u;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      const float x0 = s[nb][0] == -INFINITY ? 0.f : ex2(s[nb][0] - m + 8.f);
+      const float x1 = s[nb][1] == -INFINITY ? 0.f : ex2(s[nb][1] - m + 8.f);
+      l += x0 + x1;
+      const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3);
+      const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      const __nv_fp8x2_storage_t l2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(x0 - back.x, x1 - back.y), __NV_SATFINITE, __NV_E4M3);
+      hi |= (uint32_t)h2 << (16 * nb);
+      lo |= (uint32_t)l2 << (16 * nb);
+    }
+    // column g: hi of head g (g < G, this lane), lo of head g - G (G <= g <
+    // 2G, the lane 4G before), else zero
+    const uint32_t lo_up = __shfl_up_sync(0xffffffffu, lo, 4 * G);
+    const uint32_t b0 = g < G ? hi : (g < 2 * G ? lo_up : 0u);
+    // ---- O^T += V^T P: ldmatrix rows are the warp's 16 keys (lanes 16..31
+    // repeat the addresses of lanes 0..15)
+    const int kr = warp * KW + ((4 * g + t) & 15);
+    const uint8_t* vrow = vs + kr * kRowBytes;
+#pragma unroll
+    for (int b = 0; b < DB; ++b) {
+      uint32_t a0, a1;
+      asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0,%1}, [%2];"
+                   : "=r"(a0), "=r"(a1)
+                   : "r"(smem_u32(vrow + 16 * (b ^ (kr & kSwizzle)))));
+      asm volatile(
+          "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[b][0]), "+f"(c[b][1]), "+f"(c[b][2]), "+f"(c[b][3])
+          : "r"(a0), "r"(a1), "r"(0u), "r"(0u), "r"(b0), "r"(0u));
+    }
+  }
+  SGL_DEV void publish(float* red_acc, float* red_m, float* red_l) {
+    constexpr float kUnscale = 1.f / 256.f;  // x and the sums carry 2^8
+    float ls = l + __shfl_xor_sync(0xffffffffu, l, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    if (g < G && t == 0) {
+      red_m[warp * G + g] = m;
+      red_l[warp * G + g] = ls * kUnscale;
+    }
+    // head h's hi and lo sit in columns h and G + h: the next lane (G = 2)
+    // or the lane two on (G = 4)
+#pragma unroll
+    for (int b = 0; b < DB; ++b) {
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = c[b][k] + __shfl_down_sync(0xffffffffu, c[b][k], G / 2);
+      if (t < G / 2) {
+        const int h0 = 2 * t;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          red_acc[(warp * G + h0 + (k & 1)) * D + 16 * b + 8 * (k >> 1) + g] = v[k] * kUnscale;
+      }
+    }
+  }
+};
+
 template <int D, int G, int LPT, typename KV>
 __host__ __device__ constexpr int split_min_blocks() {
-  return use_mma<KV, G>() ? kMmaMinBlocks : min_blocks<D, G, LPT>();
+  return use_e4m3_mma<KV, G>() ? kE4m3MinBlocks : use_mma<KV, G>() ? kMmaMinBlocks : min_blocks<D, G, LPT>();
 }
 
 // Ring shape of the split kernel: the tensor-core path takes 32 bf16 keys per
@@ -755,7 +900,7 @@ template <typename KV, int G>
 struct SplitRing {
   static constexpr bool kMma = use_mma<KV, G>();
   static constexpr int kTileB = kMma ? kTileBf16 : kTileBf16Fma;  // bf16 keys per stage
-  static constexpr int kDepth = kMma ? kStages : kStagesFma;
+  static constexpr int kDepth = use_e4m3_mma<KV, G>() ? kStagesE4m3 : kMma ? kStages : kStagesFma;
   static constexpr int kTile = kTileB * 2 / (int)sizeof(KV);            // keys per stage
   template <int D>
   static constexpr size_t bytes() { return (size_t)kDepth * 2 * kTileB * D * 2; }
@@ -779,8 +924,9 @@ SGL_DEV void split_units(const Params& p, uint8_t* smem, int32_t* s_item, int gt
   constexpr int kStages = kDepth > 0 ? kDepth : Ring::kDepth;
   constexpr int kTileBytes = kTile * L::kRowBytes;         // one K or V tile
   constexpr int kStageBytes = 2 * kTileBytes;              // K then V
-  using State = std::conditional_t<use_mma<KV, G>(), MmaState<D, G, KV, kTile>,
-                                   FmaState<D, G, LPT, KV, kTile>>;
+  using State = std::conditional_t<
+      use_e4m3_mma<KV, G>(), E4m3MmaState<D, G, kTile>,
+      std::conditional_t<use_mma<KV, G>(), MmaState<D, G, KV, kTile>, FmaState<D, G, LPT, KV, kTile>>>;
   int32_t* s_slots = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
   float* s_red = reinterpret_cast<float*>(smem);           // reuses the ring after an item
 
@@ -827,7 +973,7 @@ SGL_DEV void split_units(const Params& p, uint8_t* smem, int32_t* s_item, int gt
         const int32_t j = tile * kTile + tok;
         const bool ok = j < n;
         const int64_t row = ok ? (int64_t)s_slots[j] * p.Hkv_pool : 0;
-        const uint32_t d = st_a + tok * L::kRowBytes + vec * 16;
+        const uint32_t d = st_a + tok * L::kRowBytes + (vec ^ (tok & State::kSwizzle)) * 16;
         cp_async_16(d, kbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
         cp_async_16(d + kTileBytes, vbase + row * L::kRowBytes + vec * 16, ok ? 16u : 0u);
       }

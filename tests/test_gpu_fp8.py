@@ -101,19 +101,20 @@ def test_decode_fp8_matches_oracle(shape):
     assert_close(decode_fp8(w, pk, pv, ks, vs), oracle_fp8(w, ks, vs), f"decode fp8 {shape}")
 
 
-@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (8, 2)])
 def test_decode_fp8_wide_scores(hq, hkv):
     """Scores spread over tens of natural-log units (unit-variance q and k, a
-    large softmax scale): with two or four query heads per KV head the K
+    large softmax scale): with one, two or four query heads per KV head the K
     codes meet the query as three e4m3 terms in the tensor core, whose
-    rounding the large scores would magnify -- the output must still match."""
+    rounding the large scores would magnify, and P meets the V codes as two
+    e4m3 terms, most of them tiny -- the output must still match."""
     w = decode_case(61 + hq, Hq=hq, Hkv=hkv, D=128, seq_lens=[900, 333, 2000, 1], scale=0.8)
     ks, vs = 1.0 / 32, 1.0 / 32
     pk, pv = fp8_pools(w, 1, ks, vs)
     assert_close(decode_fp8(w, pk, pv, ks, vs), oracle_fp8(w, ks, vs), f"decode fp8 wide scores {hq}/{hkv}")
 
 
-@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8)])
 def test_decode_fp8_query_range(hq, hkv):
     """Queries whose dims span six orders of magnitude (a few dims 300x,
     half of them 1/1000x): each head's query is scaled by a power of two into
