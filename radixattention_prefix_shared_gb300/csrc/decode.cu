@@ -17,10 +17,22 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
   constexpr size_t kRing = SplitRing<KV, G>::template bytes<D>();
   constexpr size_t smem = kRing + kChunk * sizeof(int32_t);
   static_assert(kWarps * G * (D + 2) * sizeof(float) <= kRing, "reduction scratch must fit in the ring");
-  auto kern = decode_split_kernel<D, G, LPT, KV>;
-  const int blocks_per_sm = kernel_blocks_per_sm<decode_split_kernel<D, G, LPT, KV>>((int)smem, kThreads);
+  // e4m3 pools: a slot's rows of kWarps adjacent KV heads gathered as one span
+  // (spans_for)
+  constexpr bool kFp8 = sizeof(KV) == 1;
+  const bool spans = kFp8 && spans_for(prm.Hkv, prm.kv_split, true);
+  auto kern = decode_split_kernel<D, G, LPT, KV, false>;
+  int blocks_per_sm;
+  if constexpr (kFp8) {
+    if (spans) kern = decode_split_kernel<D, G, LPT, KV, true>;
+    blocks_per_sm = spans ? kernel_blocks_per_sm<decode_split_kernel<D, G, LPT, KV, true>>((int)smem, kThreads)
+                          : kernel_blocks_per_sm<decode_split_kernel<D, G, LPT, KV, false>>((int)smem, kThreads);
+  } else {
+    blocks_per_sm = kernel_blocks_per_sm<decode_split_kernel<D, G, LPT, KV, false>>((int)smem, kThreads);
+  }
   if (blocks_per_sm < 0) return SGL_ERR_CUDA;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.Hkv, prm.ws,
+  const int gy = spans ? prm.Hkv / kWarps : prm.Hkv;  // grid y: counters (heads or head groups)
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.chunk, prm.Hkv, prm.ws,
                                              gr);
   if (ga != nullptr) {
     const sgl_status st = launch_cascade_groups(*ga, stream);
@@ -29,10 +41,10 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
   // one wave of resident CTAs, every CTA taking items while any are left
   // (measured against two waves: tree cascade +5.5%, Llama-7B-like decode
   // +1.8%, chunked-mix decode kernel +1.2%)
-  int64_t gx = ((int64_t)blocks_per_sm * num_sms() + prm.Hkv - 1) / prm.Hkv;
+  int64_t gx = ((int64_t)blocks_per_sm * num_sms() + gy - 1) / gy;
   if (gx > max_items) gx = max_items;
   if (gx < 1) gx = 1;
-  kern<<<dim3((unsigned)gx, (unsigned)prm.Hkv), kThreads, smem, stream>>>(prm);
+  kern<<<dim3((unsigned)gx, (unsigned)gy), kThreads, smem, stream>>>(prm);
   const int64_t warps = (int64_t)prm.batch * prm.Hq;
   decode_combine_kernel<D><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
@@ -69,7 +81,8 @@ size_t decode_workspace_bytes(int32_t batch, int32_t max_seq_len, int32_t Hq, in
   const size_t head = cascade ? kCascadeStatusBytes : 0;
   if (batch <= 0 || max_seq_len <= 0 || Hkv <= 0 || Hq < Hkv) return head + 256;
   const int32_t split = kv_split_for(Hq / Hkv);
-  return head + ws_layout(batch, max_items_for(batch, max_seq_len), Hkv * split, Hq / Hkv / split, D,
+  const int32_t chunk = chunk_for(spans_possible(Hkv * split, split));
+  return head + ws_layout(batch, max_items_for(batch, max_seq_len, chunk), Hkv * split, Hq / Hkv / split, D,
                           cascade ? max_depth : 0, cascade, nullptr, nullptr);
 }
 

@@ -136,8 +136,8 @@ sgl_status run_mixed(const MixParams& mp, int64_t max_items, cudaStream_t stream
   static_assert(mixed_decode_built<G>(), "decode group size");
   constexpr int kSmem = ext::smem_bytes<D, false>();
   if (kernel_blocks_per_sm<mixed_kernel<D, G, LPT>>(kSmem, kMixThreads) < 0) return SGL_ERR_CUDA;
-  dec::decode_plan_kernel<<<1, 1024, 0, stream>>>(mp.d.seq_lens, mp.d.batch, max_items, mp.d.Hkv, mp.d.ws,
-                                                  dec::Groups{}, mp.counters);
+  dec::decode_plan_kernel<<<1, 1024, 0, stream>>>(mp.d.seq_lens, mp.d.batch, max_items, mp.d.chunk, mp.d.Hkv,
+                                                  mp.d.ws, dec::Groups{}, mp.counters);
   mixed_kernel<D, G, LPT><<<(unsigned)num_sms(), kMixThreads, kSmem, stream>>>(mp);
   const int64_t warps = (int64_t)mp.d.batch * mp.d.Hq;
   dec::decode_combine_kernel<D><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(mp.d);
