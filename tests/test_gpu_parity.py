@@ -118,6 +118,12 @@ DECODE_SHAPES = [
     (32, 1, 128, [900, 33]),                 # 2 x 16
     (48, 2, 128, [700, 2]),                  # 2 x 12 per KV head
     (34, 2, 64, [500, 1]),                   # 17 = 17 x 1 (prime)
+    # KV heads in groups of 4 (e4m3 pools gather a slot's 4 rows as one span;
+    # items of 512 keys): one, three and two groups, every span group size
+    (8, 4, 64, [1, 511, 512, 513, 1300]),
+    (24, 12, 128, [2049, 64, 1]),
+    (48, 12, 64, [777, 3]),
+    (8, 8, 128, [1024, 255]),
 ]
 
 
