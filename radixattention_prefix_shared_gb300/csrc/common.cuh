@@ -191,6 +191,16 @@ SGL_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abo
   }
 }
 
+// ----------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream still runs: from the moment every CTA of
+// that one has signalled (or exited).  grid_dep_wait blocks the thread until
+// the kernel before has completed and its memory writes are visible; without
+// such a dependency both return at once.
+
+SGL_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+SGL_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- named barriers
 
 SGL_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {

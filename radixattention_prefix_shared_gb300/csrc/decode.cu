@@ -32,21 +32,28 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
   }
   if (blocks_per_sm < 0) return SGL_ERR_CUDA;
   const int gy = spans ? prm.Hkv / kWarps : prm.Hkv;  // grid y: counters (heads or head groups)
+  // plan, split kernel, the cascade's group pass, combine: each launched
+  // dependent on the one before (it may start while that one runs, and
+  // waits for what it needs); the group pass reads nothing of the split
+  // kernel's and fills the SMs the split kernel's last units leave
   decode_plan_kernel<<<1, 1024, 0, stream>>>(prm.seq_lens, prm.batch, max_items, prm.chunk, prm.Hkv, prm.ws,
                                              gr);
-  if (ga != nullptr) {
-    const sgl_status st = launch_cascade_groups(*ga, stream);
-    if (st != SGL_OK) return st;
-  }
   // one wave of resident CTAs, every CTA taking items while any are left
   // (measured against two waves: tree cascade +5.5%, Llama-7B-like decode
   // +1.8%, chunked-mix decode kernel +1.2%)
   int64_t gx = ((int64_t)blocks_per_sm * num_sms() + gy - 1) / gy;
   if (gx > max_items) gx = max_items;
   if (gx < 1) gx = 1;
-  kern<<<dim3((unsigned)gx, (unsigned)gy), kThreads, smem, stream>>>(prm);
+  if (launch_dependent(kern, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), smem, stream, prm) != cudaSuccess)
+    return SGL_ERR_CUDA;
+  if (ga != nullptr) {
+    const sgl_status st = launch_cascade_groups(*ga, stream, true);
+    if (st != SGL_OK) return st;
+  }
   const int64_t warps = (int64_t)prm.batch * prm.Hq;
-  decode_combine_kernel<D><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(prm);
+  if (launch_dependent(decode_combine_kernel<D>, dim3((unsigned)((warps + 3) / 4)), dim3(128), 0, stream, prm) !=
+      cudaSuccess)
+    return SGL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
 }
 

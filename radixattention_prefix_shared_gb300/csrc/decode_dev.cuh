@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t* __rest
                                                            int32_t* counters = nullptr) {
   __shared__ int32_t warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dep_launch();  // the split kernel may start; it waits for this plan
   for (int h = tid; h < Hkv; h += blockDim.x) ws.next_item[h] = 0;
   if (counters != nullptr && tid < kMixCounters) counters[tid] = 0;
   if (ws.req_info != nullptr) {
@@ -1090,6 +1091,11 @@ decode_split_kernel(Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int32_t s_item[2];
   const int y = blockIdx.y;
+  // launched dependent on the plan: a cascade's group pass (launched
+  // dependent on this kernel) may take the SMs this grid leaves; then wait
+  // for the plan's items and counters
+  grid_dep_launch();
+  grid_dep_wait();
   split_units<D, G, LPT, KV, 0, kSpans>(
       p, smem, s_item, threadIdx.x, *p.ws.n_items, [] { __syncthreads(); },
       [&] { return atomicAdd(&p.ws.next_item[y], 1); }, [&](int32_t) { return kSpans ? kWarps * y : y; },
@@ -1100,6 +1106,7 @@ decode_split_kernel(Params p) {
 
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(Params p) {
+  grid_dep_wait();  // launched dependent on the split kernel (or the group pass)
   const int lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (gw >= (int64_t)p.batch * p.Hq) return;

@@ -23,8 +23,8 @@ sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_
 }
 
 template <int D, bool kFp8>
-sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members,
-                      cudaStream_t stream) {
+sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members, cudaStream_t stream,
+                      bool dependent) {
   // bf16 pools: one Q tile a CTA, two CTAs an SM (most groups of a tree fill
   // one tile; the second CTA's work hides each CTA's start and end)
   constexpr int kTiles = kFp8 ? 2 : kGroupTilesBf16;
@@ -35,23 +35,29 @@ sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members,
   const int per_cta = kTiles * prm.tpt;
   const unsigned gx = (unsigned)((max_members + per_cta - 1) / per_cta);
   dim3 grid(gx, (unsigned)prm.Hkv, (unsigned)n_groups);
-  kern<<<grid, kThreads, kSmem, stream>>>(prm);
+  if (dependent) {
+    if (launch_dependent(kern, grid, dim3(kThreads), kSmem, stream, prm) != cudaSuccess) return SGL_ERR_CUDA;
+  } else {
+    kern<<<grid, kThreads, kSmem, stream>>>(prm);
+  }
   return cudaGetLastError() == cudaSuccess ? SGL_OK : SGL_ERR_CUDA;
 }
 
 template <bool kFp8>
 sgl_status dispatch(int head_dim, bool groups, const Params& prm, int32_t n, int32_t max_rows,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, bool dependent = false) {
   if (head_dim == 128)
-    return groups ? run_groups<128, kFp8>(prm, n, max_rows, stream) : run<128, kFp8>(prm, n, max_rows, stream);
+    return groups ? run_groups<128, kFp8>(prm, n, max_rows, stream, dependent)
+                  : run<128, kFp8>(prm, n, max_rows, stream);
   if (head_dim == 64)
-    return groups ? run_groups<64, kFp8>(prm, n, max_rows, stream) : run<64, kFp8>(prm, n, max_rows, stream);
+    return groups ? run_groups<64, kFp8>(prm, n, max_rows, stream, dependent)
+                  : run<64, kFp8>(prm, n, max_rows, stream);
   return SGL_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
-sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
+sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream, bool dependent) {
   if (a.n_groups == 0 || a.max_members == 0) return SGL_OK;
   const int g = a.num_q_heads / a.num_kv_heads;
   if (g < 1 || g > BM) return SGL_ERR_UNSUPPORTED;
@@ -87,8 +93,8 @@ sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream) {
   prm.part_base = a.part_base;
   prm.max_depth = a.max_depth;
   prm.batch = a.batch;
-  return a.kv_fp8 ? dispatch<true>(a.head_dim, true, prm, a.n_groups, a.max_members, stream)
-                  : dispatch<false>(a.head_dim, true, prm, a.n_groups, a.max_members, stream);
+  return a.kv_fp8 ? dispatch<true>(a.head_dim, true, prm, a.n_groups, a.max_members, stream, dependent)
+                  : dispatch<false>(a.head_dim, true, prm, a.n_groups, a.max_members, stream, dependent);
 }
 
 size_t extend_workspace_bytes() { return 256; }

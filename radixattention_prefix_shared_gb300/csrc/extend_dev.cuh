@@ -1155,6 +1155,10 @@ __global__ void __launch_bounds__(Roles<kFp8>::kThreads, 1) extend_kernel(Params
 template <int D, bool kFp8, int kTiles>
 __global__ void __launch_bounds__(Roles<kFp8, kTiles>::kThreads, 3 - kTiles) cascade_group_kernel(Params p) {
   attend_tiles<D, true, kFp8, kTiles>(p, blockIdx.x, blockIdx.y, blockIdx.z);
+  // launched dependent on the decode split kernel, whose tail items it does
+  // not read: it ends only once that kernel has, so the combine launched
+  // after it finds both kernels' partial states
+  grid_dep_wait();
 }
 
 // The kernel parameters of an extend call (host checks of the shapes the

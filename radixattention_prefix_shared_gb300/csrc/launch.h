@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "../../include/sgl_attn.h"
 
@@ -121,7 +122,29 @@ struct GroupArgs {
   bool kv_fp8 = false;
   float k_scale = 1.f;
 };
-sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream);
+// dependent: launched with programmatic stream serialization (it may start
+// while the split kernel before it runs, and waits for it at its end)
+sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream, bool dependent = false);
+
+// Launches kern<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialization: the kernel may start once every CTA of the kernel
+// before it in the stream has signalled (grid_dep_launch) or exited, and
+// must call grid_dep_wait before it reads what that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct ExtendArgs {
   const void* q;
