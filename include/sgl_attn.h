@@ -220,7 +220,9 @@ sgl_status sgl_decode_attention_noalloc(const void* q, const void* pool_k, const
  * persistent launch: extend_sms SMs start on extend tiles, the others on
  * decode work, and an SM whose side has run out takes the other side's work.
  * extend_sms = 0 picks the split from the host values (half the maxima taken
- * as mean lengths); 0 < extend_sms < the SM count sets it.
+ * as mean lengths); a positive extend_sms sets it (from the SM count on, every
+ * SM starts on extend tiles).  Measured: the launch takes the same time at
+ * every split (the SMs' work adds up whichever side they start on).
  *   - The pools are bf16; the argument checks, preconditions, error codes and
  *     workspace sizes are those of the two calls (ext_workspace >=
  *     sgl_extend_workspace_bytes, its first 256 bytes zero-filled once before
