@@ -49,11 +49,17 @@ namespace dec {
 namespace {
 
 constexpr int kChunk = 1024;   // keys per work item (the most an item holds)
-// keys per work item when a unit covers kWarps KV heads (span gathers);
-// measured against 256 and 1024 (e4m3: chunked mix, Llama-7B-like, tree
-// decode best at 512 -- shorter items add partial states for the combine,
-// longer ones leave too few units to even out the last round)
+// keys per work item when a unit covers kWarps KV heads (span gathers).
+// Shorter items add partial states for the combine, longer ones leave too
+// few units to even out the last round.  e4m3 tokens/s against 512-key items
+// (measured): 384 keys -2% to -8%; 768 keys +4.4% on the tree cascade (its
+// ~520-key private tails become one item each), +1.1% on the chunked mix
+// (contexts up to 32 K), -2.7% on Llama-7B-like (64 requests of 0.5-4 K)
+// and -0.9% on the tree's plain decode.  A call takes 768-key items for a
+// cascade's tails or when max_seq_len reaches kLongSeq, else 512.
 constexpr int kSpanChunk = 512;
+constexpr int kSpanChunkLong = 768;
+constexpr int kLongSeq = 16384;
 constexpr int kTileBf16 = 32;  // tensor-core path: bf16 keys per pipeline stage (twice as many e4m3)
 constexpr int kStages = 4;     // tensor-core path: ring depth
 // the CUDA-core path (measured best there: a deeper ring of smaller tiles)
@@ -146,7 +152,7 @@ struct Params {
   // pool's own KV head count (the row stride of a slot).
   int32_t batch, Hq, Hkv;
   int32_t kv_split, Hkv_pool;
-  int32_t chunk;  // keys per work item (kChunk, or kSpanChunk with span gathers)
+  int32_t chunk;  // keys per work item (kChunk; with span gathers kSpanChunk or kSpanChunkLong)
   float scale_log2;  // softmax scale * log2(e) * K scale (1 for a bf16 pool)
   float v_scale;     // V scale of an e4m3 pool (1 for bf16), applied to the output
   Ws ws;
@@ -1161,7 +1167,7 @@ inline int32_t kv_split_for(int32_t G) {
 // heads as one span (512 bytes at head dim 128 instead of four 128-byte rows:
 // random 128-byte rows read at 4.6-4.8 TB/s on this part, 512-byte spans at
 // 6.9) when its (kernel) KV heads come in whole groups of kWarps, each its
-// own pool head; its items then hold kSpanChunk keys.  Measured with e4m3
+// own pool head; its items then hold kSpanChunk or kSpanChunkLong keys.  Measured with e4m3
 // pools: chunked mix +3.9%, Llama-7B-like +4.0%, tree cascade +3.2% (tokens
 // a second).  bf16 pools keep one KV head a unit (256-byte rows already read
 // at 6.6-6.8 TB/s; spans measured +1.0% on the chunked mix, -0.6% on
@@ -1169,7 +1175,11 @@ inline int32_t kv_split_for(int32_t G) {
 // too few span units).  spans_possible: the bound the workspace is sized for.
 inline bool spans_possible(int32_t Hkv, int32_t kv_split) { return kv_split == 1 && Hkv % kWarps == 0; }
 inline bool spans_for(int32_t Hkv, int32_t kv_split, bool kv_fp8) { return kv_fp8 && spans_possible(Hkv, kv_split); }
-inline int32_t chunk_for(bool spans) { return spans ? kSpanChunk : kChunk; }
+inline int32_t chunk_for(bool spans) { return spans ? kSpanChunk : kChunk; }  // the shortest a call takes
+inline int32_t chunk_for(bool spans, bool cascade, int32_t max_seq_len) {
+  if (!spans) return kChunk;
+  return cascade || max_seq_len >= kLongSeq ? kSpanChunkLong : kSpanChunk;
+}
 
 // The kernel parameters of a decode call: the workspace layout and, for a
 // cascade decode, the group pass's arguments.
@@ -1186,7 +1196,7 @@ inline sgl_status make_decode_params(const DecodeArgs& a, Params* prm, DecodePla
   const int G = G_pool / split;                 // query heads of a (virtual) KV head
   const int Hkv = a.num_kv_heads * split;       // KV heads as the kernels see them
   const int64_t max_items = max_items_for(a.batch, a.max_seq_len, chunk_for(spans_possible(Hkv, split)));
-  prm->chunk = chunk_for(spans_for(Hkv, split, a.kv_fp8));
+  prm->chunk = chunk_for(spans_for(Hkv, split, a.kv_fp8), a.cascade, a.max_seq_len);
   prm->q = static_cast<const __nv_bfloat16*>(a.q);
   prm->pool_k = static_cast<const uint8_t*>(a.pool_k);
   prm->pool_v = static_cast<const uint8_t*>(a.pool_v);
