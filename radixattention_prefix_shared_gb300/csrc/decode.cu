@@ -15,7 +15,7 @@ sgl_status run(const Params& prm, int64_t max_items, const Groups& gr, const Gro
                cudaStream_t stream) {
   constexpr int LPT = (D == 128 && G >= 4) ? 16 : 8;
   constexpr size_t kRing = SplitRing<KV, G>::template bytes<D>();
-  constexpr size_t smem = kRing + kChunk * sizeof(int32_t);
+  constexpr size_t smem = kRing + kItemMax * sizeof(int32_t);
   static_assert(kWarps * G * (D + 2) * sizeof(float) <= kRing, "reduction scratch must fit in the ring");
   // e4m3 pools: a slot's rows of kWarps adjacent KV heads gathered as one span
   // (spans_for)

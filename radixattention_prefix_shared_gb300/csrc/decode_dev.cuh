@@ -48,7 +48,13 @@ namespace sgl {
 namespace dec {
 namespace {
 
-constexpr int kChunk = 1024;   // keys per work item (the most an item holds)
+// keys per work item: kChunk, or kChunkLong when max_seq_len reaches
+// kLongSeq (chunked-mix decode 6,705 -> 6,782 GB/s, tree decode unchanged;
+// 2,048-key items cost Llama-7B-like decode 28%: too few items); kItemMax is
+// the most any item holds (the slot run's shared-memory buffer)
+constexpr int kChunk = 1024;
+constexpr int kChunkLong = 1536;
+constexpr int kItemMax = 1536;
 // keys per work item when a unit covers kWarps KV heads (span gathers).
 // Shorter items add partial states for the combine, longer ones leave too
 // few units to even out the last round.  e4m3 tokens/s against 512-key items
@@ -60,6 +66,7 @@ constexpr int kChunk = 1024;   // keys per work item (the most an item holds)
 constexpr int kSpanChunk = 512;
 constexpr int kSpanChunkLong = 768;
 constexpr int kLongSeq = 16384;
+static_assert(kChunkLong <= kItemMax && kSpanChunkLong <= kItemMax, "slot run buffer");
 constexpr int kTileBf16 = 32;  // tensor-core path: bf16 keys per pipeline stage (twice as many e4m3)
 constexpr int kStages = 4;     // tensor-core path: ring depth
 // the CUDA-core path (measured best there: a deeper ring of smaller tiles)
@@ -152,7 +159,7 @@ struct Params {
   // pool's own KV head count (the row stride of a slot).
   int32_t batch, Hq, Hkv;
   int32_t kv_split, Hkv_pool;
-  int32_t chunk;  // keys per work item (kChunk; with span gathers kSpanChunk or kSpanChunkLong)
+  int32_t chunk;  // keys per work item (chunk_for)
   float scale_log2;  // softmax scale * log2(e) * K scale (1 for a bf16 pool)
   float v_scale;     // V scale of an e4m3 pool (1 for bf16), applied to the output
   Ws ws;
@@ -1177,7 +1184,7 @@ inline bool spans_possible(int32_t Hkv, int32_t kv_split) { return kv_split == 1
 inline bool spans_for(int32_t Hkv, int32_t kv_split, bool kv_fp8) { return kv_fp8 && spans_possible(Hkv, kv_split); }
 inline int32_t chunk_for(bool spans) { return spans ? kSpanChunk : kChunk; }  // the shortest a call takes
 inline int32_t chunk_for(bool spans, bool cascade, int32_t max_seq_len) {
-  if (!spans) return kChunk;
+  if (!spans) return max_seq_len >= kLongSeq ? kChunkLong : kChunk;
   return cascade || max_seq_len >= kLongSeq ? kSpanChunkLong : kSpanChunk;
 }
 

@@ -50,7 +50,7 @@ constexpr int dec_group_bytes() {
   using Ring = dec::SplitRing<__nv_bfloat16, G>;
   constexpr size_t ring = (size_t)kDecDepth * 2 * Ring::kTileB * D * 2;
   static_assert(dec::kWarps * G * (D + 2) * sizeof(float) <= ring, "reduction scratch fits in the ring");
-  return (int)((ring + dec::kChunk * sizeof(int32_t) + 1023) / 1024 * 1024);
+  return (int)((ring + dec::kItemMax * sizeof(int32_t) + 1023) / 1024 * 1024);
 }
 
 // the decode state must fit the extend roles' register budget (96 a thread):
