@@ -75,13 +75,21 @@ constexpr int kGroupTilesBf16 = 1;
 // (measured: 2 staging slots -15%, half-tile staging units with 4 stages -9%)
 constexpr int kFp8Stages = 3;
 constexpr int kFp8RawSlots = 3;
-constexpr int kFp8Batch = 4;
+constexpr int kFp8Batch = 5;
 
-// warp roles: softmax warps, producer warps, the MMA warp
-// (e4m3: three producer warps; with whole-row softmax 12 warps leave 168
-// registers a thread).  kTiles: Q tiles of 128 rows a CTA (2, ping-pong; 1
-// for the cascade group pass over bf16 pools, small enough for two CTAs an
-// SM)
+// registers a thread the e4m3 kernels are built with (checked before their
+// launch: the register split below is exact for it)
+constexpr int kSplitLaunchRegs = 128;
+
+// warp roles: softmax warps, producer warps, the MMA warp.  e4m3: seven
+// producer warps (each K/V code is copied and widened by the producers, the
+// kernel's limit), 16 warps launched at 128 registers a thread and split by
+// warpgroup with setmaxnreg -- the two softmax warpgroups (whole rows) take
+// 160, the producers' and the MMA warp's give up to 96 -- against three
+// producers in 12 warps at 168 (extend 785 -> 1,062 TFLOP/s on the chunked
+// mix, 803 -> 1,034 on the shared prompt).  kTiles: Q tiles of 128 rows a CTA
+// (2, ping-pong; 1 for the cascade group pass over bf16 pools, small enough
+// for two CTAs an SM)
 template <bool kFp8, int kTiles = 2>
 struct Roles {
   // softmax: on e4m3 pools 8 warps owning whole rows (one thread a row, all
@@ -91,7 +99,13 @@ struct Roles {
   // instead of four)
   static constexpr bool kFullRows = kFp8;
   static constexpr int kSoftmaxWarps = (kFullRows ? 4 : 8) * kTiles;
-  static constexpr int kProducerWarps = kFp8 ? 3 : 2;
+  static constexpr int kProducerWarps = kFp8 ? 7 : 2;
+  // e4m3 register split (setmaxnreg.inc / .dec after the setup barrier):
+  // 8 x 32 x 160 + 8 x 32 x 96 = 65,536 = the launch's 512 threads x 128,
+  // so the increase always finds the registers the decrease releases
+  // (measured: 168 / 88 -2%, 152 / 104 -1%, 144 / 112 -3%)
+  static constexpr bool kSplitRegs = kFp8;
+  static constexpr int kSoftmaxRegs = 160, kOtherRegs = 96;
   static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kProducerThreads = kProducerWarps * 32;
@@ -640,6 +654,18 @@ SGL_DEV void attend_tiles(const Params& p, int bx, int by, int bz) {
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
 
+  if constexpr (R::kSplitRegs) {
+    // every warp of a warpgroup changes its registers together (the softmax
+    // warpgroups up, the others down); the kernel is built at 128 a thread
+    static_assert(R::kSoftmaxWarps % 4 == 0 && (R::kMmaWarp + 1) % 4 == 0, "whole warpgroups");
+    static_assert(R::kSoftmaxWarps * R::kSoftmaxRegs + (R::kMmaWarp + 1 - R::kSoftmaxWarps) * R::kOtherRegs <=
+                      (R::kMmaWarp + 1) * kSplitLaunchRegs, "register split within the launch's registers");
+    static_assert((R::kMmaWarp + 1) * 32 * kSplitLaunchRegs <= 65536, "launch registers fit the SM");
+    if (warp < R::kSoftmaxWarps)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kSoftmaxRegs));
+    else
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R::kOtherRegs));
+  }
   if (R::kFullRows && warp < R::kSoftmaxWarps) {
     if constexpr (R::kFullRows) {
     // ------------------------------------------------------------ softmax (whole rows)

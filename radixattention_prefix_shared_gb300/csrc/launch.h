@@ -126,6 +126,23 @@ struct GroupArgs {
 // while the split kernel before it runs, and waits for it at its end)
 sgl_status launch_cascade_groups(const GroupArgs& a, cudaStream_t stream, bool dependent = false);
 
+// Whether kernel Kern was built with at least `regs` registers a thread (its
+// launch allocation; read once).  A kernel that moves registers between its
+// warpgroups with setmaxnreg needs exactly the launch registers it was split
+// for: with fewer the increase would wait forever, so it is not launched.
+template <auto Kern>
+bool kernel_regs_at_least(int regs) {
+  static std::atomic<int> cache{0};
+  int r = cache.load(std::memory_order_relaxed);
+  if (r == 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, Kern) != cudaSuccess) return false;
+    r = fa.numRegs;
+    cache.store(r, std::memory_order_relaxed);
+  }
+  return r >= regs;
+}
+
 // Launches kern<<<grid, block, smem, stream>>>(args...) with programmatic
 // stream serialization: the kernel may start once every CTA of the kernel
 // before it in the stream has signalled (grid_dep_launch) or exited, and
