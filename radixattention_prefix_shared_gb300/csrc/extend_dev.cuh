@@ -1017,7 +1017,7 @@ SGL_DEV void attend_tiles(const Params& p, int bx, int by, int bz) {
 #pragma unroll
       for (int i = 0; i < kRowsPerThread; ++i) {
         const int j = b * BN + rbase + kRowStep * i;
-        dst[i] = (b < nb_pre && j < pfx) ? rtt[j] : -1;
+        dst[i] = (b < nb_pre && j < pfx && rbase + kRowStep * i < BN) ? rtt[j] : -1;
       }
     };
     if (nb_pre > 0) load_slots(0, slot_next);
@@ -1040,6 +1040,7 @@ SGL_DEV void attend_tiles(const Params& p, int bx, int by, int bz) {
 #pragma unroll
         for (int i = 0; i < kRowsPerThread; ++i) {
           const int row = rbase + kRowStep * i;
+          if (row >= BN) break;  // rows of a block: kRowStep x kRowsPerThread may exceed it
           const bool valid = slot_cur[i] >= 0;
           const __nv_bfloat16* src =
               pool + ((int64_t)(valid ? slot_cur[i] : 0) * p.Hkv + kvh) * D + ci * 8;
@@ -1053,6 +1054,7 @@ SGL_DEV void attend_tiles(const Params& p, int bx, int by, int bz) {
 #pragma unroll
         for (int i = 0; i < kRowsPerThread; ++i) {
           const int row = rbase + kRowStep * i;
+          if (row >= BN) break;
           const int j = j0 + row;
           const bool valid = j < q_end;
           const __nv_bfloat16* src =
