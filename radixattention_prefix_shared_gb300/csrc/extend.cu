@@ -15,7 +15,7 @@ sgl_status run(const Params& prm, int32_t batch, int32_t max_extend, cudaStream_
   constexpr int kSmem = smem_bytes<D, kFp8>();
   auto kern = extend_kernel<D, kFp8>;
   if (kernel_blocks_per_sm<extend_kernel<D, kFp8>>(kSmem, kThreads) < 0) return SGL_ERR_CUDA;
-  if (Roles<kFp8>::kSplitRegs && !kernel_regs_at_least<extend_kernel<D, kFp8>>(kSplitLaunchRegs))
+  if (Roles<kFp8>::kSplitRegs && !kernel_regs_at_least<extend_kernel<D, kFp8>>(Roles<kFp8>::kLaunchRegs))
     return SGL_ERR_UNSUPPORTED;
   const int per_cta = 2 * prm.tpt;
   const unsigned gx = (unsigned)((max_extend + per_cta - 1) / per_cta);
@@ -34,7 +34,8 @@ sgl_status run_groups(const Params& prm, int32_t n_groups, int32_t max_members, 
   constexpr int kSmem = smem_bytes<D, kFp8, kTiles>();
   auto kern = cascade_group_kernel<D, kFp8, kTiles>;
   if (kernel_blocks_per_sm<cascade_group_kernel<D, kFp8, kTiles>>(kSmem, kThreads) < 0) return SGL_ERR_CUDA;
-  if (Roles<kFp8, kTiles>::kSplitRegs && !kernel_regs_at_least<cascade_group_kernel<D, kFp8, kTiles>>(kSplitLaunchRegs))
+  if (Roles<kFp8, kTiles>::kSplitRegs &&
+      !kernel_regs_at_least<cascade_group_kernel<D, kFp8, kTiles>>(Roles<kFp8, kTiles>::kLaunchRegs))
     return SGL_ERR_UNSUPPORTED;
   const int per_cta = kTiles * prm.tpt;
   const unsigned gx = (unsigned)((max_members + per_cta - 1) / per_cta);

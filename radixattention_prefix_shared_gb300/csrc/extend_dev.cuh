@@ -77,19 +77,27 @@ constexpr int kFp8Stages = 3;
 constexpr int kFp8RawSlots = 3;
 constexpr int kFp8Batch = 5;
 
-// registers a thread the e4m3 kernels are built with (checked before their
-// launch: the register split below is exact for it)
-constexpr int kSplitLaunchRegs = 128;
+// registers a thread the kernels that split their registers are built with
+// (16 warps over an e4m3 pool: 128; 20 warps over a bf16 pool: 96), checked
+// before their launch: the split below is exact for it
+template <bool kFp8>
+constexpr int split_launch_regs() { return kFp8 ? 128 : 96; }
 
-// warp roles: softmax warps, producer warps, the MMA warp.  e4m3: seven
-// producer warps (each K/V code is copied and widened by the producers, the
-// kernel's limit), 16 warps launched at 128 registers a thread and split by
-// warpgroup with setmaxnreg -- the two softmax warpgroups (whole rows) take
-// 160, the producers' and the MMA warp's give up to 96 -- against three
-// producers in 12 warps at 168 (extend 785 -> 1,062 TFLOP/s on the chunked
-// mix, 803 -> 1,034 on the shared prompt).  kTiles: Q tiles of 128 rows a CTA
-// (2, ping-pong; 1 for the cascade group pass over bf16 pools, small enough
-// for two CTAs an SM)
+// warp roles: softmax warps, producer warps, the MMA warp, with registers
+// moved between warpgroups by setmaxnreg after the setup barrier (not in the
+// mixed batch kernel's persistent tiles, whose warps run decode work too).
+// e4m3: seven producer warps (each K/V code is copied and widened by the
+// producers, the kernel's limit), 16 warps launched at 128 registers a
+// thread -- the two softmax warpgroups (whole rows) take 160, the producers'
+// and the MMA warp's give up to 96 -- against three producers in 12 warps at
+// 168 (extend 785 -> 1,062 TFLOP/s on the chunked mix, 803 -> 1,034 on the
+// shared prompt).  bf16, two Q tiles: three producer warps, 20 warps
+// launched at 96 -- the four softmax warpgroups take 104, the producers' and
+// the MMA warp's give up to 64 -- against two producers in 19 warps at 96
+// (1,221 -> 1,277 TFLOP/s on the chunked mix, 1,186 -> 1,236 on the shared
+// prompt).  kTiles: Q tiles of 128 rows a CTA (2, ping-pong; 1 for the
+// cascade group pass over bf16 pools, small enough for two CTAs an SM, no
+// split)
 template <bool kFp8, int kTiles = 2>
 struct Roles {
   // softmax: on e4m3 pools 8 warps owning whole rows (one thread a row, all
@@ -99,13 +107,15 @@ struct Roles {
   // instead of four)
   static constexpr bool kFullRows = kFp8;
   static constexpr int kSoftmaxWarps = (kFullRows ? 4 : 8) * kTiles;
-  static constexpr int kProducerWarps = kFp8 ? 7 : 2;
-  // e4m3 register split (setmaxnreg.inc / .dec after the setup barrier):
-  // 8 x 32 x 160 + 8 x 32 x 96 = 65,536 = the launch's 512 threads x 128,
-  // so the increase always finds the registers the decrease releases
-  // (measured: 168 / 88 -2%, 152 / 104 -1%, 144 / 112 -3%)
-  static constexpr bool kSplitRegs = kFp8;
-  static constexpr int kSoftmaxRegs = 160, kOtherRegs = 96;
+  static constexpr int kProducerWarps = kFp8 ? 7 : (kTiles == 2 ? 3 : 2);
+  // register split (setmaxnreg.inc / .dec after the setup barrier), exact
+  // for the launch's registers so the increase always finds what the
+  // decrease releases: e4m3 8 x 32 x 160 + 8 x 32 x 96 = 512 x 128 (measured:
+  // 168 / 88 -2%, 152 / 104 -1%, 144 / 112 -3%); bf16 16 x 32 x 104 +
+  // 4 x 32 x 64 = 640 x 96
+  static constexpr bool kSplitRegs = kFp8 || kTiles == 2;
+  static constexpr int kSoftmaxRegs = kFp8 ? 160 : 104, kOtherRegs = kFp8 ? 96 : 64;
+  static constexpr int kLaunchRegs = split_launch_regs<kFp8>();
   static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
   static constexpr int kThreads = (kMmaWarp + 1) * 32;
   static constexpr int kProducerThreads = kProducerWarps * 32;
@@ -654,13 +664,14 @@ SGL_DEV void attend_tiles(const Params& p, int bx, int by, int bz) {
   const uint32_t tmem = bars->tmem_base;
   const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV);
 
-  if constexpr (R::kSplitRegs) {
+  if constexpr (R::kSplitRegs && !kPersistent) {
     // every warp of a warpgroup changes its registers together (the softmax
-    // warpgroups up, the others down); the kernel is built at 128 a thread
+    // warpgroups up, the others down); the kernel is built at kLaunchRegs a
+    // thread (checked by the launcher)
     static_assert(R::kSoftmaxWarps % 4 == 0 && (R::kMmaWarp + 1) % 4 == 0, "whole warpgroups");
     static_assert(R::kSoftmaxWarps * R::kSoftmaxRegs + (R::kMmaWarp + 1 - R::kSoftmaxWarps) * R::kOtherRegs <=
-                      (R::kMmaWarp + 1) * kSplitLaunchRegs, "register split within the launch's registers");
-    static_assert((R::kMmaWarp + 1) * 32 * kSplitLaunchRegs <= 65536, "launch registers fit the SM");
+                      (R::kMmaWarp + 1) * R::kLaunchRegs, "register split within the launch's registers");
+    static_assert((R::kMmaWarp + 1) * 32 * R::kLaunchRegs <= 65536, "launch registers fit the SM");
     if (warp < R::kSoftmaxWarps)
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R::kSoftmaxRegs));
     else
