@@ -93,8 +93,13 @@ def test_extend_validation(cuda_lib):
 def test_decode_validation_and_workspace_size(cuda_lib):
     d = _dims(num_q_heads=16, num_kv_heads=8)
     need = B.decode_workspace_bytes(248, 32768, d)
-    # partial accumulators dominate: items of up to 1,024 keys, 32 per 32,768-key request
-    assert need > 248 * 32 * 8 * 2 * 128 * 4
+    # partial accumulators dominate: 8 KV heads come in groups of 4, so a call
+    # may take 512-key items (e4m3 span units): 64 per 32,768-key request
+    assert need > 248 * 64 * 8 * 2 * 128 * 4
+    # KV heads not in groups of 4: items of 1,024 keys at the least
+    d6 = _dims(num_q_heads=12, num_kv_heads=6)
+    need6 = B.decode_workspace_bytes(248, 32768, d6)
+    assert 248 * 32 * 6 * 2 * 128 * 4 < need6 < 248 * 64 * 6 * 2 * 128 * 4
     f = cuda_lib.sgl_decode_attention
 
     def call(**kw):
@@ -237,3 +242,31 @@ def test_wait_limit_setter_returns_the_previous_limit():
     assert lib.sgl_set_device_wait_limit_ns(12345) == default
     assert lib.sgl_set_device_wait_limit_ns(0) == 12345
     assert lib.sgl_set_device_wait_limit_ns(0) == default
+
+
+def test_mixed_validation(cuda_lib):
+    """sgl_mixed_attention checks both batches' arguments (the extend's, then
+    the decode's) and its SM split before anything is launched."""
+    d = _dims(num_q_heads=16, num_kv_heads=8)
+    need = B.decode_workspace_bytes(2, 64, d)
+    f = cuda_lib.sgl_mixed_attention
+
+    def call(dims=d, **kw):
+        a = dict(qe=FAKE, k=FAKE, v=FAKE, erpi=FAKE, pl=FAKE, el=FAKE, eb=2, total=10, max_e=6, max_p=30,
+                 oe=FAKE, ews=FAKE, ewsb=256, qd=FAKE, drpi=FAKE, sl=FAKE, db=2, max_s=64, od=FAKE,
+                 dws=FAKE, dwsb=need, pk=FAKE, pv=FAKE, rtt=FAKE, rows=4, stride=64, sms=-1)
+        a.update(kw)
+        return f(a["qe"], a["k"], a["v"], a["erpi"], a["pl"], a["el"], a["eb"], a["total"], a["max_e"],
+                 a["max_p"], a["oe"], a["ews"], a["ewsb"], a["qd"], a["drpi"], a["sl"], a["db"], a["max_s"],
+                 a["od"], a["dws"], a["dwsb"], a["pk"], a["pv"], a["rtt"], a["rows"], a["stride"], a["sms"],
+                 ctypes.byref(dims) if dims is not None else None, None)
+    assert call(eb=0, db=0, sms=0) == 0                  # both batches empty: nothing to launch
+    assert call() == 1                                   # extend_sms < 0
+    assert call(dims=None) == 1
+    assert call(qe=None) == 1                            # extend argument
+    assert call(max_e=11) == 1                           # max_extend above total_extend
+    assert call(ews=None) == 3                           # extend workspace
+    assert call(sl=None) == 1                            # decode argument
+    assert call(max_s=0) == 1
+    assert call(dwsb=need - 1) == 3                      # decode workspace
+    assert call(dims=_dims(head_dim=32)) == 2
